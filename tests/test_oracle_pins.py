@@ -1,0 +1,357 @@
+"""Pins for the CPU oracle: values fixed by the hspZ pages or by mathematics.
+
+Nothing here re-types the oracle's own loops.  Each test checks the oracle
+against something independent of it: the worked example printed in "C. Hit
+discovery", brute-force enumeration, closed forms, textbook maximum prefix
+sums, hand-computed cases, numpy's own f32 rounding, or invariants the pages
+state in words.  Several cases use an asymmetric matrix so that a transposed
+operand cannot hide behind a symmetric one.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+PATTERN = "1110100110010101111"
+CARE = [i for i, c in enumerate(PATTERN) if c == "1"]
+SPAN = len(PATTERN)
+DIAG_HOXD70 = {0: 91, 1: 100, 2: 100, 3: 91}
+
+
+def hoxd70():
+    m = np.full((5, 5), -100, dtype=np.int32)
+    m[:4, :4] = [[91, -114, -31, -123], [-114, 100, -125, -31], [-31, -125, 100, -114], [-123, -31, -114, 91]]
+    return m
+
+
+def _golden():
+    rows = {}
+    slots = {}
+    with open(os.path.join(HERE, "golden", "hit_discovery_worked_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *vals = line.split()
+            vals = [int(v) for v in vals]
+            if key == "slots":
+                slots[vals[0]] = vals[1:]
+            else:
+                rows[key] = vals
+    return rows, slots
+
+
+# ---------------------------------------------------------------- hit discovery
+
+def _worked_index():
+    """A 4-bucket index whose buckets hold 0, 3, 1 and 5 reference ends."""
+    idx = np.array([0, 3, 4, 9], dtype=np.uint32)  # inclusive bucket ends
+    pos = np.array([110, 111, 112, 220, 330, 331, 332, 333, 334], dtype=np.uint32)
+    buckets = np.array([0, 1, 2, -1, 3], dtype=np.int64)  # seed 3 has no k-mer
+    return idx, pos, buckets
+
+
+def test_worked_example_counts_and_prefix():
+    rows, _ = _golden()
+    idx, pos, buckets = _worked_index()
+    cnt = oracle.count_hits(idx, buckets)
+    assert cnt.tolist() == rows["counts"]
+    P, total, rc = oracle.inclusive_prefix(cnt)
+    assert rc == 0
+    assert P.tolist() == rows["prefix"]
+    assert total == rows["prefix"][-1]
+
+
+def test_worked_example_backward_slots():
+    rows, slots = _golden()
+    idx, pos, buckets = _worked_index()
+    P = np.array(rows["prefix"], dtype=np.uint32)
+    anchors = oracle.expand(idx, pos, buckets, P, [0, 5, 0, 9], span=SPAN)
+    assert anchors.shape == (9, 2)
+    for s, want in slots.items():
+        start = int(idx[buckets[s] - 1]) if buckets[s] > 0 else 0
+        for j, slot in enumerate(want):
+            assert anchors[slot, 0] == pos[start + j]
+            assert anchors[slot, 1] == s + SPAN - 1
+    # a chunk that starts at seed 2 (hit 3) shifts every slot down by its start
+    sub = oracle.expand(idx, pos, buckets, P, [2, 5, 3, 9], span=SPAN)
+    full = anchors[3:9]
+    assert np.array_equal(sub, full)
+    # one by one
+    one = oracle.anchors_at(idx, pos, buckets, P, range(9), span=SPAN)
+    assert np.array_equal(one, anchors)
+
+
+def _kmer_match(ref, qry, r, q):
+    for c in CARE:
+        a, b = ref[r + c], qry[q + c]
+        if a > 3 or b > 3 or a != b:
+            return False
+    return True
+
+
+def _low_complexity(rng, n, n_frac=0.01):
+    s = rng.choice(np.array([0, 1], dtype=np.uint8), size=n, p=[0.6, 0.4])
+    s[rng.random(n) < 0.03] = 2
+    s[rng.random(n) < 0.02] = 3
+    s[rng.random(n) < n_frac] = 4
+    return s.astype(np.uint8)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_anchors_equal_brute_force_matches(seed):
+    rng = np.random.default_rng(seed)
+    ref = _low_complexity(rng, 500)
+    qry = _low_complexity(rng, 260)
+    qry[100:160] = ref[300:360]  # a planted copy
+    pairs = [(r + SPAN - 1, q + SPAN - 1)
+             for q in range(len(qry) - SPAN + 1)
+             for r in range(len(ref) - SPAN + 1)
+             if _kmer_match(ref, qry, r, q)]
+    # raw order: query end ascending, and within a seed the reference end descending
+    pairs.sort(key=lambda t: (t[1], -t[0]))
+    assert len(pairs) > 20
+    res = oracle.run_path(ref, qry, hoxd70(), 910, 3000)
+    assert res["rc"] == 0
+    assert res["total"] == len(pairs)
+    got = res["per_chunk"][0]["anchors"]
+    assert [tuple(map(int, a)) for a in got] == pairs
+    per_seed = np.zeros(len(qry) - SPAN + 1, dtype=np.int64)
+    for _, qe in pairs:
+        per_seed[qe - SPAN + 1] += 1
+    assert res["cnt"].tolist() == per_seed.tolist()
+
+
+def test_index_lists_every_window_once_in_ascending_bucket_runs():
+    rng = np.random.default_rng(7)
+    ref = _low_complexity(rng, 400, n_frac=0.02)
+    idx, pos = oracle.build_index(ref, PATTERN)
+    windows = [r for r in range(len(ref) - SPAN + 1) if all(ref[r + c] < 4 for c in CARE)]
+    assert sorted(pos.tolist()) == [r + SPAN - 1 for r in windows]
+    assert int(idx[-1]) == len(windows)
+    assert np.all(np.diff(idx.astype(np.int64)) >= 0)
+    starts = np.concatenate([[0], idx[:-1]]).astype(np.int64)
+    for h in np.flatnonzero(idx.astype(np.int64) - starts):
+        run = pos[starts[h]:idx[h]]
+        assert np.all(np.diff(run.astype(np.int64)) > 0)
+        # every window in one bucket run shares its care bases
+        r0 = int(run[0]) - SPAN + 1
+        for e in run[1:]:
+            assert _kmer_match(ref, ref, r0, int(e) - SPAN + 1)
+
+
+def test_refusal_edge_at_2_pow_32():
+    # all-A reference and query: every window of both falls in bucket 0.
+    ref = np.zeros(65_554, dtype=np.uint8)
+    # 65,536 reference windows x 65,536 query seeds = 2^32 hits: refused
+    res = oracle.run_path(ref, np.zeros(65_554, dtype=np.uint8), hoxd70(), 910, 3000, max_hits=1 << 20,
+                          index=oracle.build_index(ref))
+    assert res["rc"] == oracle.ORC_E_OVERFLOW
+    # one seed fewer: 2^32 - 65,536 hits, accepted (plan only)
+    idx, pos = oracle.build_index(ref)
+    b = oracle.seed_buckets(np.zeros(65_553, dtype=np.uint8))
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, b))
+    assert rc == 0 and total == (1 << 32) - 65_536
+
+
+# ---------------------------------------------------------------- chunk walk
+
+@pytest.mark.parametrize("seed", range(6))
+def test_chunk_walk_invariants(seed):
+    rng = np.random.default_rng(100 + seed)
+    S = int(rng.integers(1, 400))
+    cnt = rng.integers(0, 9, S).astype(np.uint32)
+    cnt[rng.random(S) < 0.4] = 0
+    if seed == 0:
+        cnt[-20:] = 0  # trailing zero-count seeds
+    P, total, rc = oracle.inclusive_prefix(cnt)
+    assert rc == 0
+    for cap in sorted({1, 2, 3, 5, 8, 13, 40, max(1, total // 3), max(1, total), total + 1}):
+        ch = oracle.chunk_walk(P, cap).astype(np.int64)
+        assert ch[0, 0] == 0 and ch[-1, 1] == S and ch[0, 2] == 0 and ch[-1, 3] == total
+        assert np.all(ch[1:, 0] == ch[:-1, 1]) and np.all(ch[1:, 2] == ch[:-1, 3])
+        assert np.all(ch[:, 1] > ch[:, 0])
+        for sb, se, hb, he in ch:
+            assert hb == (int(P[sb - 1]) if sb else 0) and he == int(P[se - 1])  # no seed is split
+        if total <= cap:
+            assert len(ch) == 1
+        for k, (sb, se, hb, he) in enumerate(ch):
+            if k < len(ch) - 1:
+                assert he - hb >= cap  # a cut chunk reaches the cap ...
+                assert he - hb - int(cnt[se - 1]) < cap  # ... and overruns it by less than its last seed
+            else:  # the last chunk either fits the cap or is cut at the last seed
+                assert he - hb <= cap or he - hb - int(cnt[se - 1]) < cap
+        # concatenated chunk expansions equal the unchunked stream
+        idx = np.concatenate([[0], np.cumsum(np.arange(1, 10))]).astype(np.uint32)[1:]
+        buckets = np.where(cnt > 0, cnt.astype(np.int64) - 1, -1)
+        pos = np.arange(int(idx[-1]), dtype=np.uint32) * 7
+        whole = oracle.expand(idx, pos, buckets, P, [0, S, 0, total])
+        parts = [oracle.expand(idx, pos, buckets, P, c) for c in ch.astype(np.uint32)]
+        assert np.array_equal(np.concatenate(parts) if parts else whole[:0], whole)
+
+
+# ---------------------------------------------------------------- X-drop walks
+
+def _seq(s):
+    return np.array(["ACGTN".index(c) for c in s], dtype=np.uint8)
+
+
+@pytest.mark.parametrize("a", [0, 1, 57, 298, 299])
+def test_all_match_closed_form(a):
+    rng = np.random.default_rng(a)
+    s = rng.integers(0, 4, 300).astype(np.uint8)
+    m = hoxd70()
+    sc = oracle.side_scores(s, s, [[a, a]], m, 910)[0]
+    left = sum(DIAG_HOXD70[int(b)] for b in s[:a])
+    right = sum(DIAG_HOXD70[int(b)] for b in s[a:])
+    assert sc.tolist() == [left, a, right, 300 - a]
+    rec, done = oracle.materialize(s, s, [[a, a]], 0, [0], m, 910, 3000)
+    assert rec[0].tolist() == [0, 0, 299, left + right] and done[0] == 1
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_infinite_xdrop_is_max_prefix_sum(seed):
+    rng = np.random.default_rng(seed)
+    L = 120
+    ref = rng.integers(0, 5, L).astype(np.uint8)
+    qry = np.where(rng.random(L) < 0.6, ref, rng.integers(0, 5, L)).astype(np.uint8)
+    m = rng.integers(-60, 61, (5, 5)).astype(np.int32)  # asymmetric on purpose
+    a = int(rng.integers(0, L))
+    sc = oracle.side_scores(ref, qry, [[a, a]], m, 1 << 30)[0]
+    # brute force over every (l, r) window [a-l, a+r) around the anchor
+    best, arg = None, None
+    for l in range(a + 1):
+        for r in range(L - a + 1):
+            tot = sum(int(m[ref[k], qry[k]]) for k in range(a - l, a + r))
+            if best is None or tot > best:
+                best, arg = tot, (l, r)
+    assert sc[0] + sc[2] == best
+    # the earliest maximum on each side is the smallest extent that attains it
+    assert (sc[1], sc[3]) == arg
+
+
+def _hand_matrix():
+    m = np.full((5, 5), -100, dtype=np.int32)
+    m[0, 0] = 10   # A/A
+    m[0, 1] = -10  # ref A vs query C
+    m[1, 0] = 40   # ref C vs query A: asymmetric on purpose
+    m[2, 2] = 50   # G/G
+    m[1, 1] = -25  # C/C
+    m[3, 3] = -35  # T/T
+    m[2, 3] = 100  # ref G vs query T
+    return m
+
+
+def test_drop_is_strictly_beyond_x():
+    m = _hand_matrix()
+    # right side from the anchor: +10, -10, -10, +50, then -100
+    ref = _seq("T" + "AAAGT")
+    qry = _seq("A" + "ACCGA")
+    sc = oracle.side_scores(ref, qry, [[1, 1]], m, 20)[0]
+    # S = 10, 0, -10 (deficit exactly X: the walk goes on), 40, -60 (stop)
+    assert sc[2:].tolist() == [40, 4]
+    sc = oracle.side_scores(ref, qry, [[1, 1]], m, 19)[0]
+    assert sc[2:].tolist() == [10, 1]
+
+
+def test_earliest_maximum_wins_on_ties():
+    m = _hand_matrix()
+    # right: +10, -10, +10 (ties the maximum later), then -100
+    ref = _seq("T" + "AAAT")
+    qry = _seq("A" + "ACAA")
+    sc = oracle.side_scores(ref, qry, [[1, 1]], m, 500)[0]
+    assert sc[2:].tolist() == [10, 1]
+    # left mirror: bases before the anchor at 4 are (from the anchor outward) +10, -10, +10, -100
+    ref = _seq("TAAA" + "T")
+    qry = _seq("AACA" + "A")
+    sc = oracle.side_scores(ref, qry, [[4, 4]], m, 500)[0]
+    assert sc[:2].tolist() == [10, 1]
+    rec, done = oracle.materialize(ref, qry, [[4, 4]], 0, [0], m, 500, 5)
+    assert rec[0].tolist() == [3, 3, 0, 10] and done[0] == 1
+
+
+def test_anchor_base_belongs_to_the_right_side():
+    m = _hand_matrix()
+    # right side, anchor base included: C/C -25, T/T -35, ref G/query T +100, ref A/query C -10
+    ref = _seq("AC" + "CTG" + "A")
+    qry = _seq("CC" + "CTT" + "C")
+    sc = oracle.side_scores(ref, qry, [[2, 2]], m, 70)[0]
+    # right: S = -25, -60 (deficit 60 <= 70), +40 -> max 40 at 3 bases; then ref A/qry C -10 -> 30
+    # left: ref C/qry C -25 (deficit 25), then ref A/qry C -10 -> -35, edge: max 0
+    assert sc.tolist() == [0, 0, 40, 3]
+    # had the anchor base belonged to the left side the right maximum would be 65
+    rec, done = oracle.materialize(ref, qry, [[2, 2]], 0, [0], m, 70, 40)
+    assert rec[0].tolist() == [2, 2, 2, 40] and done[0] == 1
+
+
+def test_matrix_rows_are_reference_bases():
+    m = _hand_matrix()
+    ref = _seq("C")
+    qry = _seq("A")
+    assert oracle.side_scores(ref, qry, [[0, 0]], m, 100)[0, 2] == 40
+    assert oracle.side_scores(qry, ref, [[0, 0]], m, 100)[0, 2] == 0  # ref A vs query C is -10
+
+
+def test_n_scores_by_matrix_and_edges_stop():
+    m = hoxd70()
+    ref = _seq("ACGNNACG")
+    qry = _seq("ACGTAACG")
+    sc = oracle.side_scores(ref, qry, [[0, 0]], m, 1000)[0]
+    # right: 91, 100, 100, N/T -100, N/A -100, 91, 100, 100, then the sequence edge
+    pref = np.cumsum([91, 100, 100, -100, -100, 91, 100, 100])
+    assert sc[2] == pref.max() and sc[3] == int(np.argmax(pref)) + 1
+
+
+# ---------------------------------------------------------------- threshold
+
+def test_keep_threshold_matches_f32_compare():
+    rng = np.random.default_rng(5)
+    Ks = [1, 2, 3000, (1 << 24) - 1, 1 << 24, (1 << 24) + 1, (1 << 24) + 3, (1 << 25) + 5,
+          123_456_789, (1 << 31) - 1] + rng.integers(1, 1 << 31, 40).tolist()
+    for K in Ks:
+        T = oracle.keep_threshold(K)
+        assert 1 <= T <= K
+        fK = np.float32(K)
+        assert np.float32(T) >= fK
+        assert T == 1 or np.float32(T - 1) < fK
+        if K <= (1 << 24):
+            assert T == K
+    for K in range(1, 3000, 97):
+        assert oracle.keep_threshold(K) == K
+    with pytest.raises(oracle.OracleError):
+        oracle.keep_threshold(0)
+
+
+# ---------------------------------------------------------------- compaction / materialize
+
+def test_compaction_is_stable_and_global():
+    rng = np.random.default_rng(9)
+    flags = (rng.random(10_001) < 0.03).astype(np.uint8)
+    ids = oracle.compact(flags, 12345)
+    assert np.array_equal(ids, np.flatnonzero(flags).astype(np.uint32) + 12345)
+    assert oracle.compact(np.zeros(0, np.uint8)).size == 0
+
+
+def test_materialized_records_score_their_closed_interval():
+    from seed_hits_ungapped_gb300 import synth
+    w = synth.make("tiny", scale=0.1)
+    res = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K)
+    m = w.matrix
+    seen = 0
+    for ch in res["per_chunk"]:
+        ids, rec, done = ch["ids"], ch["rec"], ch["done"]
+        assert np.array_equal(ids, np.flatnonzero(ch["flags"]).astype(np.uint32) + int(res["chunks"][0][2]))
+        sides = oracle.side_scores(w.ref, w.query, ch["anchors"][ids], m, w.xdrop)
+        for k in range(ids.size):
+            rs, qs, ln, score = map(int, rec[k])
+            diag = [int(m[w.ref[rs + t], w.query[qs + t]]) for t in range(ln + 1)]
+            assert sum(diag) == score == sides[k, 0] + sides[k, 2]
+            assert done[k] == (score >= res["T"])
+            a_r, a_q = map(int, ch["anchors"][ids[k]])
+            assert a_r - rs == a_q - qs == sides[k, 1]  # the left extent shifts both starts
+            assert ln + 1 == sides[k, 1] + sides[k, 3]
+            seen += 1
+    assert seen > 100
