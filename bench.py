@@ -1,0 +1,361 @@
+"""Benchmark: seed hits -> anchors -> score gate -> survivors -> SegmentPairs.
+
+One step = the whole path over one synthetic query batch: hit discovery
+(count, prefix, chunk walk), fused expansion + score gate, stable compaction,
+materialization and the accepted compaction.  The metric is anchors per
+second; the dominant kernel (fused expansion + gate) is also reported against
+the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+With N > 1 the script runs under torchrun, one rank per GPU; every rank runs
+its own copy of the workload (weak scaling) and rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "anchors/sec (hit expansion + score gate, device-timed); HBM GB/s vs GB300 peak"
+UNIT = "anchors/s"
+L2_FLUSH_BYTES = 512 << 20
+
+WORKLOAD_DESC = {
+    "workload_a": "workload_a: ref 100 Mbp + query 25 Mbp at 41% GC, 10,000 planted homologies 100-3000 bp at "
+                  "5-25% divergence, 12of19 seed, HOXD70, X-drop 910, K 3000, one chunk",
+    "tiny": "tiny: ref 1 Mbp + query 200 kbp uniform, 100 homologies 200-2000 bp at 10%",
+    "mid": "mid: ref 20 Mbp + query 5 Mbp at 41% GC with 1% N runs, 2,000 homologies 100-5000 bp at 5-30%",
+    "dense": "dense: ref 10 Mbp + query 2 Mbp with a 300 bp repeat (5,000/1,000 copies) and 2% (CA)n",
+    "chunking": "chunking: workload_a + 4 kbp poly-A, both strands, MAX_HITS 2^24",
+}
+
+
+def algorithmic_bytes(n_seeds: int, n_anchors: int, ref_len: int, qry_len: int) -> int:
+    """Compulsory bytes of the fused expansion + gate: 16 per seed (two index
+    reads, the prefix, the bucket start), 13 per anchor (4-byte position read,
+    8-byte anchor write, 1-byte flag write), and both sequences once."""
+    return 16 * n_seeds + 13 * n_anchors + ref_len + qry_len
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def run_cpu_baseline(w, seconds: float = 12.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of the
+    same workload: expansion + gate over the seeds of the query's leading
+    part (index, counts and prefix are set up untimed)."""
+    import oracle
+    idx, pos = oracle.build_index(w.ref)
+    buckets = oracle.seed_buckets(w.query)
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
+    T = oracle.keep_threshold(w.K)
+    done_anchors, t_used, s_begin = 0, 0.0, 0
+    step_seeds = 200_000
+    while t_used < seconds and s_begin < P.size:
+        s_end = min(P.size, s_begin + step_seeds)
+        hb = int(P[s_begin - 1]) if s_begin else 0
+        chunk = np.array([s_begin, s_end, hb, P[s_end - 1]], np.uint32)
+        t0 = time.perf_counter()
+        a = oracle.expand(idx, pos, buckets, P, chunk)
+        oracle.gate(w.ref, w.query, a, w.matrix, w.xdrop, T)
+        t_used += time.perf_counter() - t0
+        done_anchors += len(a)
+        s_begin = s_end
+    return {"value": done_anchors / t_used, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "expansion + gate of the first %d seeds (%d anchors) of the %s query, single-threaded C"
+                      % (s_begin, done_anchors, w.name), "seconds": round(t_used, 3)}
+
+
+def reference_arm(args):
+    """--impl reference: the oracle, timed on the host cores, on bounded samples."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from seed_hits_ungapped_gb300 import synth
+    import oracle
+    w = synth.make(args.workload)
+    idx, pos = oracle.build_index(w.ref)
+    buckets = oracle.seed_buckets(w.query)
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
+    T = oracle.keep_threshold(w.K)
+    sample_seeds = 400_000
+    times, anchors = [], 0
+    for step in range(args.warmup + args.steps):
+        s0 = (step * sample_seeds) % max(1, P.size - sample_seeds)
+        s1 = min(P.size, s0 + sample_seeds)
+        hb = int(P[s0 - 1]) if s0 else 0
+        chunk = np.array([s0, s1, hb, P[s1 - 1]], np.uint32)
+        t0 = time.perf_counter()
+        a = oracle.expand(idx, pos, buckets, P, chunk)
+        f = oracle.gate(w.ref, w.query, a, w.matrix, w.xdrop, T)
+        ids = oracle.compact(f, hb)
+        oracle.materialize(w.ref, w.query, a, hb, ids, w.matrix, w.xdrop, T)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            anchors += len(a)
+    value = anchors / sum(times)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic", "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": "per step: expansion + gate + compaction + materialization of %d "
+                                       "consecutive seeds of the %s query (single-threaded C oracle)"
+                                       % (sample_seeds, w.name)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="workload_a")
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return reference_arm(args)
+
+    import torch
+    import torch.distributed as dist
+    from seed_hits_ungapped_gb300 import hspz, synth
+    from seed_hits_ungapped_gb300.engine import HspEngine
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    w = synth.make(args.workload)
+    lib = hspz.load_library()
+    eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
+    stream = torch.cuda.current_stream()
+    d_queries = [torch.from_numpy(q).cuda() for q in w.queries]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    ev_gate = []
+
+    def step(timed_gate=False):
+        """One pass of the whole path over every query batch of the workload."""
+        n_anchors = n_seeds = 0
+        for dq in d_queries:
+            plan = eng.plan(dq, w.max_hits)
+            n_seeds += plan.n_seeds
+            for c in range(plan.n_chunks):
+                hb, he = int(plan.chunks[c, 2]), int(plan.chunks[c, 3])
+                n = he - hb
+                anchors = eng.buffer("anchors", n, torch.int32, 2)
+                flags = eng.buffer("flags", n, torch.uint8)
+                if timed_gate:
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                hspz.hspz_expand_gate(plan, c, eng.params, anchors, flags)
+                if timed_gate:
+                    e1.record(stream)
+                    ev_gate.append((e0, e1, n))
+                ids, n_surv = eng._compact(flags, n, hb, "ids")
+                rec = eng.buffer("records", n_surv, torch.int32, 4)
+                done = eng.buffer("done", n_surv, torch.uint8)
+                hspz.hspz_materialize(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
+                eng._compact(done, n_surv, 0, "accepted")
+                n_anchors += n
+            plan.close()
+        return n_anchors, n_seeds
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+
+    # timed region: K steps, each bracketed by CUDA events on the launching
+    # stream, with an L2 flush between steps outside the events
+    step_ms = []
+    launches0 = lib.hspz_kernel_launches()
+    with ClockSampler(local) as clocks:
+        barrier()
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            n_anchors, n_seeds = step(timed_gate=True)
+            b.record(stream)
+            b.synchronize()
+            step_ms.append(a.elapsed_time(b))
+        barrier()
+        t_wall = time.perf_counter() - t_wall0
+    launches = lib.hspz_kernel_launches() - launches0
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * n_anchors * args.steps / (total_ms / 1e3)
+
+    # dominant kernel: fused expansion + gate (one launch per chunk), CUDA-event time per launch
+    gate_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev_gate]
+    n_launch = len(gate_ms)
+    step_bytes = algorithmic_bytes(n_seeds, n_anchors, w.ref.size * len(w.queries), sum(q.size for q in w.queries))
+    alg_bytes_per_launch = step_bytes * args.steps / n_launch
+    achieved = step_bytes * args.steps / (sum(gate_ms) / 1e3) / 1e9
+    peak, peak_kind = measured_peaks()
+    traffic = None
+    tp = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tp):
+        try:
+            tr = json.load(open(tp))
+            if tr.get("workload") == args.workload and tr.get("kernel_rev") == kernel_rev():
+                traffic = tr.get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pinned = [torch.from_numpy(q).pin_memory() for q in w.queries]
+        e2e_ms = []
+        h2d = sum(q.numel() for q in pinned)
+        d2h = 0
+        for it in range(args.warmup + max(3, args.steps // 2)):
+            flush.zero_()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            d2h = 0
+            for pq in pinned:
+                dq = pq.to("cuda", non_blocking=True)
+                res = eng.run(dq, max_hits=w.max_hits)
+                # the step's result: accepted records, done flags and accepted ids to host
+                for c in res.per_chunk:
+                    rec = eng._bufs["records"][: c.n_survivors].cpu()
+                    dn = eng._bufs["done"][: c.n_survivors].cpu()
+                    acc = eng._bufs["accepted"][: c.n_accepted].cpu()
+                    d2h += rec.numel() * 4 + dn.numel() + acc.numel() * 4
+            torch.cuda.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(1e3 * (time.perf_counter() - t0))
+        e2e = {"value": n_anchors / (statistics.median(e2e_ms) / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": statistics.median(e2e_ms)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = run_cpu_baseline(w)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    res = eng.run(d_queries[0], max_hits=w.max_hits)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload), "anchors_per_step": n_anchors,
+                   "seeds_per_step": n_seeds, "survivors": res.n_survivors, "accepted": res.n_accepted,
+                   "chunks": int(len(res.chunks)), "l2": "flushed (512 MiB write) between timed steps",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "kernel": "k_expand_gate (fused expansion + score gate)",
+                     "kernel_ms_per_launch": sum(gate_ms) / n_launch,
+                     "algorithmic_bytes_per_launch": alg_bytes_per_launch},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def kernel_rev() -> str:
+    """Content hash of the CUDA sources (ties stored ncu traffic to a kernel version)."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "seed_hits_ungapped_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        h.update(open(os.path.join(d, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+if __name__ == "__main__":
+    sys.exit(main())

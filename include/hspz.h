@@ -1,0 +1,226 @@
+/*
+ * hspz.h -- C ABI of the GB300 (sm_103a) seed-hit -> ungapped X-drop HSP library.
+ *
+ * The library turns query spaced seeds into raw (reference-end, query-end)
+ * anchors against a bucketed reference k-mer index, gates every anchor with an
+ * exact score-only X-drop test, compacts the survivors stably and materializes
+ * them into 16-byte SegmentPair records.  The operations follow the hspZ
+ * v0.0.4 documentation:
+ *   "C. Hit discovery"          C.1 count, C.2 prefix, C.3 MAX_HITS chunks,
+ *                               C.4 sparse/dense choice, C.5 backward expansion
+ *   "D. Score gate"             D.1 anchor feed, D.2 score-only X-drop + keep
+ *                               threshold, D.3 byte flags, D.4 stable compaction
+ *   "E. X-drop materialization" E.1 restore, E.2 right, E.3 left, E.4 closed
+ *                               interval, E.5 store
+ *
+ * Conventions for every call
+ *   - Base codes are uint8: A=0 C=1 G=2 T=3; any other value is N.
+ *   - The substitution matrix is int32[25], row = reference base, column =
+ *     query base, index 5*ref + query (row/column 4 = N).
+ *   - Coordinates are 0-based.  An anchor holds the END of its seed window:
+ *     reference end = window start + span - 1, query end = seed index + span - 1
+ *     (seed s is the query window starting at position s; every query position
+ *     is seeded).
+ *   - Pointers named d_* are DEVICE pointers on the current CUDA device and
+ *     stay owned by the caller.  Pointers without the prefix are host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are stream ordered; a call that returns counts to the
+ *     host (hspz_build_index, hspz_find_hits, hspz_compact) synchronizes that
+ *     stream before it returns.
+ *   - Every call returns an hspz_status.  A non-zero status means no output
+ *     of that call was written, except the *_needed / total counts documented
+ *     below.  Arguments are checked before any launch; hspz_strerror() names
+ *     the status, hspz_last_error() gives the last detailed message.
+ *   - Every output slot a call owns is overwritten in full (the pages' "every
+ *     active flag slot is overwritten before reuse", D.3, and "every active
+ *     output slot is fully overwritten", E.5).
+ *   - Limits: 1 <= K <= 2^30, 0 <= xdrop <= 2^30, |matrix entry| <= 2^16,
+ *     sequences shorter than 2^32 - 2^10 bases.
+ */
+#ifndef HSPZ_H
+#define HSPZ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HSPZ_ABI_VERSION 1
+
+typedef enum hspz_status {
+    HSPZ_OK = 0,
+    HSPZ_E_INVAL = 1,        /* bad argument (null pointer, bad pattern, limits)     */
+    HSPZ_E_HIT_OVERFLOW = 2, /* total hits do not fit the 32-bit hit index (C.2)     */
+    HSPZ_E_CAPACITY = 3,     /* output capacity too small; the needed size is given  */
+    HSPZ_E_CUDA = 4,         /* a CUDA runtime call failed (see hspz_last_error)     */
+    HSPZ_E_NOMEM = 5,        /* device or host allocation failed                      */
+    HSPZ_E_UNSUPPORTED = 6   /* request outside what this build implements           */
+} hspz_status;
+
+/* Packed anchor, raw hit order (D.1 "packed (reference-end, query-end) anchors"). 8 bytes. */
+typedef struct hspz_anchor {
+    uint32_t ref_end;
+    uint32_t query_end;
+} hspz_anchor;
+
+/* Materialized HSP (E.4/E.5): the closed interval ref_start..=ref_start+len on
+ * the reference and query_start..=query_start+len on the query; score is the
+ * substitution-score sum over that interval.  16 bytes, 16-byte aligned. */
+typedef struct hspz_segment_pair {
+    uint32_t ref_start;
+    uint32_t query_start;
+    uint32_t len;
+    int32_t score;
+} hspz_segment_pair;
+
+/* One MAX_HITS chunk (C.3): seeds [seed_begin, seed_end) and global anchor
+ * ids [hit_begin, hit_end).  A seed is never split across chunks. */
+typedef struct hspz_chunk {
+    uint32_t seed_begin;
+    uint32_t seed_end;
+    uint32_t hit_begin;
+    uint32_t hit_end;
+} hspz_chunk;
+
+/* Scoring (D.2): substitution matrix, X-drop and hsp threshold K. */
+typedef struct hspz_score_params {
+    int32_t matrix[25];
+    int32_t xdrop;
+    int32_t K;
+} hspz_score_params;
+
+typedef struct hspz_index hspz_index; /* reference side: k-mer index + packed reference   */
+typedef struct hspz_plan hspz_plan;   /* one query batch: seeds, prefix, chunks, packed query */
+
+/* Expansion mappings (C.4). */
+enum { HSPZ_EXPAND_AUTO = 0, HSPZ_EXPAND_SPARSE = 1, HSPZ_EXPAND_DENSE = 2 };
+/* hspz_find_hits flags (C.3): locate chunk boundaries by copying the whole
+ * prefix array instead of the block sums plus one 256-count block per cut. */
+enum { HSPZ_WALK_FULL = 1 };
+
+const char *hspz_strerror(int status);
+const char *hspz_last_error(void);
+int hspz_abi_version(void);
+/* Number of CUDA kernels this library has launched in this process (all
+ * devices, all threads); lets a caller count the launches of a region. */
+uint64_t hspz_kernel_launches(void);
+
+/* ------------------------------------------------------------------------ *
+ * Keep threshold ("D. Score gate", D.2 invariant): the least integer total t
+ * for which (float)t >= (float)K, i.e. the integer twin of KegAlign's f32 keep
+ * comparison; computed once per engine on the host.  Returns HSPZ_E_INVAL for
+ * K < 1 or K > 2^30.
+ * ------------------------------------------------------------------------ */
+int hspz_keep_threshold(int32_t K, int32_t *T_out);
+
+/* ------------------------------------------------------------------------ *
+ * Reference index ("C. Hit discovery", C.1 index table of cumulative bucket
+ * ends; C.5 bucket start..end).  d_ref: ref_len base codes.  seed_pattern: a
+ * string of '1' (care) and '0' (don't care), first and last '1', span <= 32,
+ * weight <= 12 (default "1110100110010101111").  Every reference window
+ * without N at a care offset is indexed by its packed k-mer (first care base
+ * most significant); the index holds idx[4^weight] (inclusive bucket ends)
+ * and pos[] (reference ends, ascending inside each bucket) plus a packed copy
+ * of the reference for scoring.  The library owns the handle; free it with
+ * hspz_index_free after every plan made from it.  Synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_build_index(const uint8_t *d_ref, uint64_t ref_len, const char *seed_pattern,
+                     hspz_index **index_out, void *stream);
+void hspz_index_free(hspz_index *index);
+/* Sizes and device views of the index tables (owned by the index). */
+int hspz_index_info(const hspz_index *index, uint64_t *n_positions, uint32_t *span, uint32_t *weight);
+int hspz_index_tables(const hspz_index *index, const uint32_t **d_idx, const uint32_t **d_pos);
+
+/* ------------------------------------------------------------------------ *
+ * Hit discovery for one query batch ("C. Hit discovery", C.1-C.3).
+ * Seeds every query window (n_seeds = query_len - span + 1), counts each
+ * seed's hits (find_num_hits: bucket end - previous bucket end; 0 for a seed
+ * with N at a care offset), forms the global inclusive prefix and the total,
+ * refuses a total above 2^32 - 1 with HSPZ_E_HIT_OVERFLOW (no plan is made;
+ * *total_hits still reports the total), and cuts MAX_HITS chunks: one chunk if
+ * total <= max_hits or max_hits == 0, else the lower-bound walk over the seed
+ * prefixes that keeps the straddling seed whole.  flags: 0 or HSPZ_WALK_FULL.
+ * The plan keeps pointers into `index`.  Synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_find_hits(const hspz_index *index, const uint8_t *d_query, uint64_t query_len, uint64_t max_hits,
+                   uint32_t flags, hspz_plan **plan_out, uint64_t *total_hits, void *stream);
+void hspz_plan_free(hspz_plan *plan);
+/* n_seeds, total hits, chunk count and the largest chunk's hit count. */
+int hspz_plan_info(const hspz_plan *plan, uint64_t *n_seeds, uint64_t *total_hits, uint32_t *n_chunks,
+                   uint64_t *max_chunk_hits);
+/* Host copy of the chunk list; HSPZ_E_CAPACITY (with *n_chunks set) if cap is too small. */
+int hspz_plan_chunks(const hspz_plan *plan, hspz_chunk *chunks, uint32_t cap, uint32_t *n_chunks);
+/* Device view of the inclusive prefix P[n_seeds] (uint32, owned by the plan). */
+int hspz_plan_prefix(const hspz_plan *plan, const uint32_t **d_prefix);
+
+/* ------------------------------------------------------------------------ *
+ * Backward expansion of one chunk ("C. Hit discovery", C.4-C.5): occurrence j
+ * of seed s (j = 0 at the bucket start) goes to slot P[s] - 1 - hit_begin - j.
+ * mode: HSPZ_EXPAND_AUTO picks the warp-per-seed mapping when the chunk holds
+ * at least 16 hits per seed, else thread-per-seed; both write identical
+ * anchors.  d_anchors needs cap >= chunk hits (else HSPZ_E_CAPACITY).
+ * ------------------------------------------------------------------------ */
+int hspz_expand(const hspz_plan *plan, uint32_t chunk, int mode, hspz_anchor *d_anchors, uint64_t cap,
+                void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Fused expansion + score gate of one chunk (C.5 + D.1-D.3): writes the same
+ * anchors as hspz_expand and, for each, the flag byte of hspz_score_gate.
+ * ------------------------------------------------------------------------ */
+int hspz_expand_gate(const hspz_plan *plan, uint32_t chunk, const hspz_score_params *params,
+                     hspz_anchor *d_anchors, uint8_t *d_flags, uint64_t cap, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Score-only X-drop gate ("D. Score gate", D.2-D.3) over n anchors against the
+ * index's reference and the plan's query.  Per anchor (a_r, a_q): the right
+ * side scores the anchor base and the bases after it, the left side the bases
+ * before it; each side walks with S_0 = M_0 = 0, S_n = S_{n-1} + m[ref][qry],
+ * stops before step n when M_{n-1} - S_n > xdrop or at a sequence edge, and
+ * yields its maximum M.  flag = (M_left + M_right >= T) with T =
+ * hspz_keep_threshold(K): 1 keeps, 0 rejects.  An anchor outside the
+ * sequences gets flag 0.
+ * ------------------------------------------------------------------------ */
+int hspz_score_gate(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors, uint64_t n,
+                    const hspz_score_params *params, uint8_t *d_flags, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Stable compaction ("D. Score gate", D.4): d_ids receives id_base + i for
+ * every i < n with d_flags[i] != 0, in increasing order; *n_out receives the
+ * count.  If the count exceeds cap nothing is written and HSPZ_E_CAPACITY is
+ * returned with *n_out set.  Uses stream-ordered scratch from the device's
+ * default memory pool.  Synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
+                 uint64_t *n_out, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Exact X-drop materialization ("E. X-drop materialization", E.1-E.5).  For
+ * survivor k with global id d_ids[k], the anchor d_anchors[d_ids[k] - id_base]
+ * (n_anchors entries; an id outside [id_base, id_base + n_anchors) yields a
+ * rejected slot) is walked right and left as in hspz_score_gate, keeping on each side the
+ * EARLIEST step count n attaining the maximum (0 for the empty prefix).  Then
+ * ref_start = a_r - n_left, query_start = a_q - n_left,
+ * len = n_left + n_right - 1 (closed interval start..=start+len) and
+ * score = M_left + M_right (saturated at INT32_MAX).  done[k] = score >= T: an
+ * accepted slot holds the record, a rejected slot is written as zeros with
+ * done = 0.  d_out must be 16-byte aligned.
+ * ------------------------------------------------------------------------ */
+int hspz_materialize(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors,
+                     uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
+                     const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Host-only chunk walk over a host prefix array, exactly the walk
+ * hspz_find_hits runs (use_block_sums != 0: lower bound located through the
+ * 256-count block sums, then inside one block; 0: over the whole array).
+ * For testing the host logic without a GPU.
+ * ------------------------------------------------------------------------ */
+int hspz_chunk_walk_host(const uint32_t *prefix, uint64_t n_seeds, uint64_t max_hits, int use_block_sums,
+                         hspz_chunk *chunks, uint32_t cap, uint32_t *n_chunks);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HSPZ_H */

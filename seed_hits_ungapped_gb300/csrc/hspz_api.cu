@@ -1,0 +1,452 @@
+// Host side of libhspz: argument checks, handles, the keep threshold, hit
+// discovery orchestration and the MAX_HITS chunk walk ("C. Hit discovery",
+// C.2-C.3), and the C ABI entry points declared in include/hspz.h.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <functional>
+#include <mutex>
+
+#include "hspz_internal.cuh"
+
+namespace hspz {
+
+cudaError_t build_index_tables(const uint8_t *d_ref, uint64_t ref_len, const SeedShape &sh, uint32_t *d_idx,
+                               uint32_t **d_pos_out, uint64_t *n_pos_out, cudaStream_t st);
+
+namespace {
+thread_local std::string g_last_error;
+constexpr uint64_t kMaxSeqLen = (1ull << 32) - 1024;
+constexpr int64_t kMaxK = 1ll << 30;
+constexpr int64_t kMaxX = 1ll << 30;
+constexpr int64_t kMaxAbsScore = 1ll << 16;
+}  // namespace
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
+
+void set_error(const std::string &msg) { g_last_error = msg; }
+
+int cuda_fail(cudaError_t e, const char *what) {
+    set_error(std::string(what) + ": " + cudaGetErrorString(e));
+    return e == cudaErrorMemoryAllocation ? HSPZ_E_NOMEM : HSPZ_E_CUDA;
+}
+
+int parse_pattern(const char *pat, SeedShape *sh) {
+    if (!pat) pat = "1110100110010101111";
+    int n = 0, w = 0;
+    for (; pat[n]; n++) {
+        if (n >= kMaxSpan) return HSPZ_E_INVAL;
+        if (pat[n] == '1') {
+            if (w >= kMaxWeight) return HSPZ_E_INVAL;
+            sh->care[w++] = n;
+        } else if (pat[n] != '0') {
+            return HSPZ_E_INVAL;
+        }
+    }
+    if (w < 1 || pat[0] != '1' || pat[n - 1] != '1') return HSPZ_E_INVAL;
+    sh->span = n;
+    sh->weight = w;
+    for (int i = w; i < kMaxSpan; i++) sh->care[i] = 0;
+    return HSPZ_OK;
+}
+
+// Keep threshold: the f32 rounding of integers is monotone, so the totals the
+// f32 comparison keeps are exactly those at or above the rounding boundary
+// between (float)K and its float predecessor.  Start from that boundary and
+// settle the tie with the compiler's own int -> float conversion.
+static int keep_threshold(int32_t K, int32_t *T) {
+    if (K < 1 || K > kMaxK) return HSPZ_E_INVAL;
+    const float f = (float)K;
+    const float prev = nextafterf(f, 0.0f);
+    const double mid = 0.5 * ((double)prev + (double)f);
+    int64_t c = (int64_t)ceil(mid);
+    while (c > 1 && (float)(c - 1) >= f) c--;
+    while ((float)c < f) c++;
+    *T = (int32_t)c;
+    return HSPZ_OK;
+}
+
+int make_score_args(const hspz_score_params *p, ScoreArgs *out) {
+    if (!p) return HSPZ_E_INVAL;
+    if (p->xdrop < 0 || p->xdrop > kMaxX) return HSPZ_E_INVAL;
+    for (int i = 0; i < 25; i++)
+        if (p->matrix[i] > kMaxAbsScore || p->matrix[i] < -kMaxAbsScore) return HSPZ_E_INVAL;
+    int32_t T;
+    if (keep_threshold(p->K, &T)) return HSPZ_E_INVAL;
+    memcpy(out->m, p->matrix, sizeof(out->m));
+    out->xdrop = p->xdrop;
+    out->T = T;
+    // complement-symmetric 8-entry table (see the gate kernels): entry
+    // x | parity(r) << 2 with x = r ^ q over codes A0 C1 G2 T3.
+    int8_t tab[8];
+    bool fast = true;
+    for (int r = 0; r < 4; r++)
+        for (int q = 0; q < 4; q++) {
+            int e = (r ^ q) | (((r ^ (r >> 1)) & 1) << 2);
+            int v = p->matrix[5 * r + q];
+            int vc = p->matrix[5 * (r ^ 3) + (q ^ 3)];
+            if (v != vc || v < -128 || v > 127) fast = false;
+            tab[e] = (int8_t)v;
+        }
+    if (fast && tab[0] < 0) fast = false;
+    out->tab_lo = (uint8_t)tab[0] | ((uint32_t)(uint8_t)tab[1] << 8) | ((uint32_t)(uint8_t)tab[2] << 16) |
+                  ((uint32_t)(uint8_t)tab[3] << 24);
+    out->tab_hi = (uint8_t)tab[4] | ((uint32_t)(uint8_t)tab[5] << 8) | ((uint32_t)(uint8_t)tab[6] << 16) |
+                  ((uint32_t)(uint8_t)tab[7] << 24);
+    out->fast = fast ? 1 : 0;
+    return HSPZ_OK;
+}
+
+// ------------------------------------------------------------------ chunk walk
+// "C.3": one chunk if the hits left fit the cap, else the lower bound over the
+// seed prefixes for hit_begin + cap, located through the inclusive block sums
+// (256 seeds per block) and then inside the one block that holds it; the seed
+// found there is kept whole.  fetch(b, out) copies prefix block b.
+using FetchBlock = std::function<int(uint64_t block, uint32_t *out, uint64_t *n)>;
+
+static int chunk_walk(uint64_t S, uint64_t total, uint64_t max_hits, const uint64_t *blk_incl, uint64_t nb,
+                      const uint32_t *full_P, const FetchBlock &fetch, std::vector<hspz_chunk> &out) {
+    out.clear();
+    uint64_t sb = 0, hb = 0;
+    std::vector<uint32_t> blk(kCountBlock);
+    while (sb < S) {
+        uint64_t se, he;
+        if (max_hits == 0 || total - hb <= max_hits) {
+            se = S;
+            he = total;
+        } else {
+            const uint64_t target = hb + max_hits;
+            uint64_t e;
+            if (full_P) {
+                e = (uint64_t)(std::lower_bound(full_P, full_P + S, target,
+                                                [](uint32_t a, uint64_t t) { return (uint64_t)a < t; }) -
+                               full_P);
+                he = full_P[e];
+            } else {
+                const uint64_t b = (uint64_t)(std::lower_bound(blk_incl, blk_incl + nb, target) - blk_incl);
+                if (b >= nb) return HSPZ_E_INVAL;
+                uint64_t got = 0;
+                int rc = fetch(b, blk.data(), &got);
+                if (rc) return rc;
+                const uint64_t k = (uint64_t)(std::lower_bound(blk.data(), blk.data() + got, target,
+                                                               [](uint32_t a, uint64_t t) { return (uint64_t)a < t; }) -
+                                              blk.data());
+                if (k >= got) return HSPZ_E_INVAL;
+                e = b * kCountBlock + k;
+                he = blk[k];
+            }
+            se = e + 1;
+        }
+        out.push_back(hspz_chunk{(uint32_t)sb, (uint32_t)se, (uint32_t)hb, (uint32_t)he});
+        sb = se;
+        hb = he;
+    }
+    return HSPZ_OK;
+}
+
+}  // namespace hspz
+
+using namespace hspz;
+
+// ---------------------------------------------------------------- C ABI
+extern "C" {
+
+const char *hspz_strerror(int status) {
+    switch (status) {
+        case HSPZ_OK: return "ok";
+        case HSPZ_E_INVAL: return "invalid argument";
+        case HSPZ_E_HIT_OVERFLOW: return "total hits exceed the 32-bit hit index";
+        case HSPZ_E_CAPACITY: return "output capacity too small";
+        case HSPZ_E_CUDA: return "CUDA error";
+        case HSPZ_E_NOMEM: return "out of memory";
+        case HSPZ_E_UNSUPPORTED: return "unsupported";
+        default: return "unknown status";
+    }
+}
+
+const char *hspz_last_error(void) { return g_last_error.c_str(); }
+
+int hspz_abi_version(void) { return HSPZ_ABI_VERSION; }
+
+uint64_t hspz_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int hspz_keep_threshold(int32_t K, int32_t *T_out) {
+    if (!T_out) return HSPZ_E_INVAL;
+    return keep_threshold(K, T_out);
+}
+
+int hspz_build_index(const uint8_t *d_ref, uint64_t ref_len, const char *seed_pattern, hspz_index **index_out,
+                     void *stream) {
+    if (!index_out || (!d_ref && ref_len) || ref_len > kMaxSeqLen) return HSPZ_E_INVAL;
+    *index_out = nullptr;
+    SeedShape sh;
+    if (parse_pattern(seed_pattern, &sh)) {
+        set_error("bad seed pattern");
+        return HSPZ_E_INVAL;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    hspz_index *ix = new (std::nothrow) hspz_index();
+    if (!ix) return HSPZ_E_NOMEM;
+    ix->shape = sh;
+    ix->ref_len = ref_len;
+    cudaGetDevice(&ix->device);
+    const uint64_t nb = 1ull << (2 * sh.weight);
+    ix->ref_words = packed_words(ref_len);
+    cudaError_t e = cudaMalloc((void **)&ix->d_idx, nb * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref, ix->ref_words * 4);
+    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, ix->d_ref, ix->ref_words, st);
+    if (e == cudaSuccess) e = build_index_tables(d_ref, ref_len, sh, ix->d_idx, &ix->d_pos, &ix->n_pos, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(e, "hspz_build_index");
+        hspz_index_free(ix);
+        return rc;
+    }
+    *index_out = ix;
+    return HSPZ_OK;
+}
+
+void hspz_index_free(hspz_index *ix) {
+    if (!ix) return;
+    if (ix->d_idx) cudaFree(ix->d_idx);
+    if (ix->d_pos) cudaFree(ix->d_pos);
+    if (ix->d_ref) cudaFree(ix->d_ref);
+    delete ix;
+}
+
+int hspz_index_info(const hspz_index *ix, uint64_t *n_positions, uint32_t *span, uint32_t *weight) {
+    if (!ix) return HSPZ_E_INVAL;
+    if (n_positions) *n_positions = ix->n_pos;
+    if (span) *span = (uint32_t)ix->shape.span;
+    if (weight) *weight = (uint32_t)ix->shape.weight;
+    return HSPZ_OK;
+}
+
+int hspz_index_tables(const hspz_index *ix, const uint32_t **d_idx, const uint32_t **d_pos) {
+    if (!ix) return HSPZ_E_INVAL;
+    if (d_idx) *d_idx = ix->d_idx;
+    if (d_pos) *d_pos = ix->d_pos;
+    return HSPZ_OK;
+}
+
+void hspz_plan_free(hspz_plan *p) {
+    if (!p) return;
+    for (void *q : {(void *)p->d_P, (void *)p->d_lo, (void *)p->d_cnt, (void *)p->d_blk, (void *)p->d_qry})
+        if (q) cudaFree(q);
+    delete p;
+}
+
+int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_len, uint64_t max_hits,
+                   uint32_t flags, hspz_plan **plan_out, uint64_t *total_hits, void *stream) {
+    if (!ix || !plan_out || (!d_query && query_len) || query_len > kMaxSeqLen || (flags & ~1u)) return HSPZ_E_INVAL;
+    *plan_out = nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    hspz_plan *p = new (std::nothrow) hspz_plan();
+    if (!p) return HSPZ_E_NOMEM;
+    p->index = ix;
+    p->query_len = query_len;
+    const int span = ix->shape.span;
+    const uint64_t S = query_len >= (uint64_t)span ? query_len - span + 1 : 0;
+    p->n_seeds = S;
+    const uint64_t nb = (S + kCountBlock - 1) / kCountBlock;
+    p->n_blocks = nb;
+    p->qry_words = packed_words(query_len);
+    cudaError_t e = cudaSuccess;
+    const uint64_t sa = S ? S : 1;
+    e = cudaMalloc((void **)&p->d_P, sa * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_lo, sa * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_cnt, sa * 4);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_blk, (3 * nb + 1) * 8);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_qry, p->qry_words * 4);
+    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, p->d_qry, p->qry_words, st);
+    uint64_t *bsum = p->d_blk, *bexcl = p->d_blk + nb, *bincl = p->d_blk + 2 * nb, *dtot = p->d_blk + 3 * nb;
+    if (e == cudaSuccess && S) e = launch_count(d_query, S, ix->shape, ix->d_idx, p->d_cnt, p->d_lo, bsum, st);
+    if (e == cudaSuccess && S) e = launch_scan_u64(bsum, nb, bexcl, bincl, dtot, st);
+    if (e == cudaSuccess && S) e = launch_prefix(p->d_cnt, S, bexcl, p->d_P, st);
+    uint64_t total = 0;
+    if (e == cudaSuccess && S) e = cudaMemcpyAsync(&total, dtot, 8, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(e, "hspz_find_hits");
+        hspz_plan_free(p);
+        return rc;
+    }
+    if (total_hits) *total_hits = total;
+    if (total > 0xFFFFFFFFull) {  // C.2: refused, never wrapped
+        set_error("total hits exceed the 32-bit hit index");
+        hspz_plan_free(p);
+        return HSPZ_E_HIT_OVERFLOW;
+    }
+    p->total = total;
+    // C.3 chunk walk
+    std::vector<uint64_t> blk_incl;
+    std::vector<uint32_t> full;
+    const bool cut = max_hits != 0 && total > max_hits;
+    int rc = HSPZ_OK;
+    if (cut && (flags & HSPZ_WALK_FULL)) {
+        full.resize(S);
+        e = cudaMemcpyAsync(full.data(), p->d_P, S * 4, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    } else if (cut) {
+        blk_incl.resize(nb);
+        e = cudaMemcpyAsync(blk_incl.data(), bincl, nb * 8, cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    if (e != cudaSuccess) {
+        rc = cuda_fail(e, "hspz_find_hits chunk walk");
+        hspz_plan_free(p);
+        return rc;
+    }
+    FetchBlock fetch = [&](uint64_t b, uint32_t *out, uint64_t *n) -> int {
+        const uint64_t s0 = b * kCountBlock;
+        const uint64_t cnt = std::min<uint64_t>(kCountBlock, S - s0);
+        cudaError_t e2 = cudaMemcpyAsync(out, p->d_P + s0, cnt * 4, cudaMemcpyDeviceToHost, st);
+        if (e2 == cudaSuccess) e2 = cudaStreamSynchronize(st);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "chunk walk block copy");
+        *n = cnt;
+        return HSPZ_OK;
+    };
+    rc = chunk_walk(S, total, max_hits, blk_incl.empty() ? nullptr : blk_incl.data(), nb,
+                    full.empty() ? nullptr : full.data(), fetch, p->chunks);
+    if (rc) {
+        hspz_plan_free(p);
+        return rc;
+    }
+    p->max_chunk_hits = 0;
+    for (const auto &c : p->chunks)
+        p->max_chunk_hits = std::max<uint64_t>(p->max_chunk_hits, (uint64_t)c.hit_end - c.hit_begin);
+    *plan_out = p;
+    return HSPZ_OK;
+}
+
+int hspz_plan_info(const hspz_plan *p, uint64_t *n_seeds, uint64_t *total_hits, uint32_t *n_chunks,
+                   uint64_t *max_chunk_hits) {
+    if (!p) return HSPZ_E_INVAL;
+    if (n_seeds) *n_seeds = p->n_seeds;
+    if (total_hits) *total_hits = p->total;
+    if (n_chunks) *n_chunks = (uint32_t)p->chunks.size();
+    if (max_chunk_hits) *max_chunk_hits = p->max_chunk_hits;
+    return HSPZ_OK;
+}
+
+int hspz_plan_chunks(const hspz_plan *p, hspz_chunk *chunks, uint32_t cap, uint32_t *n_chunks) {
+    if (!p || !n_chunks) return HSPZ_E_INVAL;
+    *n_chunks = (uint32_t)p->chunks.size();
+    if (cap < p->chunks.size()) return HSPZ_E_CAPACITY;
+    if (!p->chunks.empty()) {
+        if (!chunks) return HSPZ_E_INVAL;
+        memcpy(chunks, p->chunks.data(), p->chunks.size() * sizeof(hspz_chunk));
+    }
+    return HSPZ_OK;
+}
+
+int hspz_plan_prefix(const hspz_plan *p, const uint32_t **d_prefix) {
+    if (!p || !d_prefix) return HSPZ_E_INVAL;
+    *d_prefix = p->d_P;
+    return HSPZ_OK;
+}
+
+int hspz_expand(const hspz_plan *p, uint32_t chunk, int mode, hspz_anchor *d_anchors, uint64_t cap, void *stream) {
+    if (!p || chunk >= p->chunks.size() || mode < 0 || mode > 2) return HSPZ_E_INVAL;
+    const hspz_chunk &c = p->chunks[chunk];
+    const uint64_t hits = (uint64_t)c.hit_end - c.hit_begin;
+    if (cap < hits) return HSPZ_E_CAPACITY;
+    if (hits && !d_anchors) return HSPZ_E_INVAL;
+    const uint64_t seeds = (uint64_t)c.seed_end - c.seed_begin;
+    // C.4: warp-per-seed when the chunk averages at least 16 hits per seed
+    const int dense = mode == HSPZ_EXPAND_DENSE || (mode == HSPZ_EXPAND_AUTO && hits >= 16 * seeds);
+    cudaError_t e = launch_expand(p->d_P, p->d_cnt, p->d_lo, p->index->d_pos, c, p->index->shape.span, dense,
+                                  d_anchors, (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_expand");
+}
+
+int hspz_expand_gate(const hspz_plan *p, uint32_t chunk, const hspz_score_params *params, hspz_anchor *d_anchors,
+                     uint8_t *d_flags, uint64_t cap, void *stream) {
+    if (!p || chunk >= p->chunks.size()) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    const hspz_chunk &c = p->chunks[chunk];
+    const uint64_t hits = (uint64_t)c.hit_end - c.hit_begin;
+    if (cap < hits) return HSPZ_E_CAPACITY;
+    if (hits && (!d_anchors || !d_flags)) return HSPZ_E_INVAL;
+    SeqView r{p->index->d_ref, p->index->ref_len}, q{p->d_qry, p->query_len};
+    cudaError_t e = launch_expand_gate(p->d_P, p->d_lo, p->index->d_pos, c, p->index->shape.span, r, q, sa,
+                                       d_anchors, d_flags, (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_expand_gate");
+}
+
+int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n,
+                    const hspz_score_params *params, uint8_t *d_flags, void *stream) {
+    if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags))) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    SeqView r{ix->d_ref, ix->ref_len}, q{p->d_qry, p->query_len};
+    cudaError_t e = launch_gate(d_anchors, n, r, q, sa, d_flags, (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate");
+}
+
+int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
+                 uint64_t *n_out, void *stream) {
+    if (!n_out || (n && !d_flags) || n > (1ull << 32) || (uint64_t)id_base + n > (1ull << 32)) return HSPZ_E_INVAL;
+    if (cap && !d_ids) return HSPZ_E_INVAL;
+    cudaStream_t st = (cudaStream_t)stream;
+    *n_out = 0;
+    if (!n) return HSPZ_OK;
+    uint32_t *scratch = nullptr;
+    const uint64_t words = compact_scratch_words(n) + 2;
+    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_compact scratch");
+    uint64_t *d_total = reinterpret_cast<uint64_t *>(scratch + ((words - 2) & ~1ull));
+    uint64_t total = 0;
+    e = launch_compact(d_flags, n, id_base, d_ids, cap, scratch, d_total, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&total, d_total, 8, cudaMemcpyDeviceToHost, st);
+    cudaError_t ef = cudaFreeAsync(scratch, st);
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_compact");
+    *n_out = total;
+    return total > cap ? HSPZ_E_CAPACITY : HSPZ_OK;
+}
+
+int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n_anchors,
+                     uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids, const hspz_score_params *params,
+                     hspz_segment_pair *d_out, uint8_t *d_done, void *stream) {
+    if (!ix || !p || p->index != ix) return HSPZ_E_INVAL;
+    if (n_ids && (!d_anchors || !d_ids || !d_out || !d_done)) return HSPZ_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    SeqView r{ix->d_ref, ix->ref_len}, q{p->d_qry, p->query_len};
+    cudaError_t e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done,
+                                       (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize");
+}
+
+int hspz_chunk_walk_host(const uint32_t *prefix, uint64_t n_seeds, uint64_t max_hits, int use_block_sums,
+                         hspz_chunk *chunks, uint32_t cap, uint32_t *n_chunks) {
+    if (!n_chunks || (n_seeds && !prefix)) return HSPZ_E_INVAL;
+    const uint64_t total = n_seeds ? prefix[n_seeds - 1] : 0;
+    const uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
+    std::vector<uint64_t> blk(nb);
+    for (uint64_t b = 0; b < nb; b++) blk[b] = prefix[std::min<uint64_t>(n_seeds - 1, b * kCountBlock + kCountBlock - 1)];
+    FetchBlock fetch = [&](uint64_t b, uint32_t *out, uint64_t *n) -> int {
+        const uint64_t s0 = b * kCountBlock;
+        *n = std::min<uint64_t>(kCountBlock, n_seeds - s0);
+        memcpy(out, prefix + s0, *n * 4);
+        return HSPZ_OK;
+    };
+    std::vector<hspz_chunk> out;
+    int rc = chunk_walk(n_seeds, total, max_hits, use_block_sums ? blk.data() : nullptr, nb,
+                        use_block_sums ? nullptr : prefix, fetch, out);
+    if (rc) return rc;
+    *n_chunks = (uint32_t)out.size();
+    if (cap < out.size()) return HSPZ_E_CAPACITY;
+    if (!out.empty()) memcpy(chunks, out.data(), out.size() * sizeof(hspz_chunk));
+    return HSPZ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,405 @@
+// Hit discovery kernels: sequence packing, reference index build, per-seed
+// hit counting (find_num_hits), the 256-count block scan, and the two
+// expansion mappings of "C. Hit discovery" (hspZ docs, C.1-C.5).
+#include "hspz_internal.cuh"
+
+namespace hspz {
+namespace {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+__device__ __forceinline__ uint32_t pack_nibble(uint32_t c, int parity) {
+    if (c > 3) return kNibN;
+    return c | (parity ? (((c ^ (c >> 1)) & 1u) << 2) : 0u);
+}
+
+// One thread per packed word: 8 bases, padded with N outside [0, len).
+__global__ void k_pack(const uint8_t *__restrict__ codes, uint64_t len, int parity, uint32_t *__restrict__ out,
+                       uint64_t words) {
+    for (uint64_t w = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; w < words;
+         w += (uint64_t)gridDim.x * blockDim.x) {
+        int64_t b0 = (int64_t)w * 8 - kPadBases;
+        uint32_t v = 0;
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            int64_t b = b0 + i;
+            uint32_t nib = kNibN;
+            if (b >= 0 && (uint64_t)b < len) nib = pack_nibble(codes[b], parity);
+            v |= nib << (4 * i);
+        }
+        out[w] = v;
+    }
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_incl_scan(T x, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        T y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_sum(T x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// find_num_hits (C.1): one thread per seed; the block also emits its 64-bit
+// count sum (C.2: 256 counts per block).
+__global__ void __launch_bounds__(kCountBlock) k_count(const uint8_t *__restrict__ q, uint64_t n_seeds, SeedShape sh,
+                                                       const uint32_t *__restrict__ idx, uint32_t *__restrict__ cnt,
+                                                       uint32_t *__restrict__ lo, uint64_t *__restrict__ bsum) {
+    __shared__ uint8_t tile[kCountBlock + kMaxSpan];
+    __shared__ uint64_t wsum[kCountBlock / 32];
+    const uint64_t s0 = blockIdx.x * (uint64_t)kCountBlock;
+    const uint64_t qlen = n_seeds + sh.span - 1;
+    for (int i = threadIdx.x; i < kCountBlock + sh.span - 1; i += blockDim.x) {
+        uint64_t p = s0 + i;
+        tile[i] = p < qlen ? q[p] : 4;
+    }
+    __syncthreads();
+    const uint64_t s = s0 + threadIdx.x;
+    uint32_t c = 0, l = 0;
+    if (s < n_seeds) {
+        uint32_t h = 0;
+        bool ok = true;
+        for (int i = 0; i < sh.weight; i++) {
+            uint32_t b = tile[threadIdx.x + sh.care[i]];
+            ok &= (b <= 3);
+            h = h * 4u + (b & 3u);
+        }
+        if (ok) {
+            l = h ? __ldg(idx + h - 1) : 0u;
+            c = __ldg(idx + h) - l;
+        }
+        cnt[s] = c;
+        lo[s] = l;
+    }
+    uint64_t v = warp_sum<uint64_t>(c);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) wsum[warp] = v;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        uint64_t t = 0;
+        for (int w = 0; w < kCountBlock / 32; w++) t += wsum[w];
+        bsum[blockIdx.x] = t;
+    }
+}
+
+// Single-CTA scan of n values (8 per thread per round): exclusive and
+// inclusive prefixes in OutT and the total.  Used for block sums.
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(1024) k_scan(const InT *__restrict__ in, uint64_t n, OutT *__restrict__ excl,
+                                               OutT *__restrict__ incl, OutT *__restrict__ total) {
+    constexpr int kItems = 8;
+    __shared__ OutT wtot[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    OutT carry = 0;
+    for (uint64_t base = 0; base < n; base += 1024ull * kItems) {
+        OutT v[kItems];
+        OutT run = 0;
+        const uint64_t i0 = base + (uint64_t)threadIdx.x * kItems;
+#pragma unroll
+        for (int k = 0; k < kItems; k++) {
+            v[k] = (i0 + k < n) ? (OutT)in[i0 + k] : (OutT)0;
+            run += v[k];
+        }
+        OutT x = warp_incl_scan<OutT>(run, lane);
+        if (lane == 31) wtot[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            OutT t = wtot[lane];
+            t = warp_incl_scan<OutT>(t, lane);
+            wtot[lane] = t;
+        }
+        __syncthreads();
+        OutT pre = carry + (warp ? wtot[warp - 1] : (OutT)0) + (x - run);
+#pragma unroll
+        for (int k = 0; k < kItems; k++) {
+            if (i0 + k < n) {
+                if (excl) excl[i0 + k] = pre;
+                pre += v[k];
+                if (incl) incl[i0 + k] = pre;
+            }
+        }
+        carry += wtot[31];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0 && total) *total = carry;
+}
+
+// Local inclusive scan of 256 counts plus the block's exclusive offset (C.2).
+__global__ void __launch_bounds__(kCountBlock) k_prefix(const uint32_t *__restrict__ cnt, uint64_t n,
+                                                        const uint64_t *__restrict__ bexcl, uint32_t *__restrict__ P) {
+    __shared__ uint64_t wtot[kCountBlock / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint64_t s = blockIdx.x * (uint64_t)kCountBlock + threadIdx.x;
+    uint64_t v = s < n ? cnt[s] : 0;
+    uint64_t x = warp_incl_scan<uint64_t>(v, lane);
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    uint64_t pre = bexcl[blockIdx.x];
+    for (int w = 0; w < warp; w++) pre += wtot[w];
+    if (s < n) P[s] = (uint32_t)(pre + x);
+}
+
+// C.5, thread-per-seed mapping: occurrence j goes to slot P[s] - 1 - hit_begin - j.
+__global__ void k_expand_sparse(const uint32_t *__restrict__ P, const uint32_t *__restrict__ cnt,
+                                const uint32_t *__restrict__ lo, const uint32_t *__restrict__ pos, uint32_t sb,
+                                uint32_t se, uint32_t hb, uint32_t span, uint2 *__restrict__ out) {
+    const uint64_t s = sb + blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
+    if (s >= se) return;
+    const uint32_t c = cnt[s];
+    if (!c) return;
+    const uint32_t end = P[s] - hb, l = lo[s], qe = (uint32_t)s + span - 1;
+    for (uint32_t j = 0; j < c; j++) out[end - 1 - j] = make_uint2(__ldg(pos + l + j), qe);
+}
+
+// C.5, warp-per-seed mapping: the warp walks one bucket coalescently; same slots.
+__global__ void k_expand_dense(const uint32_t *__restrict__ P, const uint32_t *__restrict__ cnt,
+                               const uint32_t *__restrict__ lo, const uint32_t *__restrict__ pos, uint32_t sb,
+                               uint32_t se, uint32_t hb, uint32_t span, uint2 *__restrict__ out) {
+    const uint64_t s = sb + (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32;
+    const int lane = threadIdx.x & 31;
+    if (s >= se) return;
+    const uint32_t c = cnt[s];
+    const uint32_t end = P[s] - hb, l = lo[s], qe = (uint32_t)s + span - 1;
+    for (uint32_t j = lane; j < c; j += 32) out[end - 1 - j] = make_uint2(__ldg(pos + l + j), qe);
+}
+
+// ---------------------------------------------------------------- index build
+// Valid-window flags, then (after a stable compaction of the window starts)
+// the k-mer keys, a stable LSD radix sort on 3 x 8 key bits, and the bucket
+// ends by binary search over the sorted keys.
+
+__global__ void k_window_flags(const uint8_t *__restrict__ ref, uint64_t n_win, SeedShape sh,
+                               uint8_t *__restrict__ flags) {
+    for (uint64_t r = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; r < n_win;
+         r += (uint64_t)gridDim.x * blockDim.x) {
+        bool ok = true;
+        for (int i = 0; i < sh.weight; i++) ok &= ref[r + sh.care[i]] <= 3;
+        flags[r] = ok ? 1 : 0;
+    }
+}
+
+__global__ void k_window_keys(const uint8_t *__restrict__ ref, const uint32_t *__restrict__ starts, uint64_t n,
+                              SeedShape sh, uint32_t *__restrict__ keys, uint32_t *__restrict__ vals) {
+    for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t r = starts[i];
+        uint32_t h = 0;
+        for (int k = 0; k < sh.weight; k++) h = h * 4u + (ref[(uint64_t)r + sh.care[k]] & 3u);
+        keys[i] = h;
+        vals[i] = r + (uint32_t)sh.span - 1;
+    }
+}
+
+constexpr int kRadixThreads = 256;
+constexpr int kRadixItems = 16;
+constexpr int kRadixTile = kRadixThreads * kRadixItems;
+
+// Digit histogram of one tile, stored digit-major: hist[d * n_tiles + tile].
+__global__ void __launch_bounds__(kRadixThreads) k_radix_hist(const uint32_t *__restrict__ keys, uint64_t n, int shift,
+                                                              uint32_t *__restrict__ hist, uint64_t n_tiles) {
+    __shared__ uint32_t h[256];
+    h[threadIdx.x] = 0;
+    __syncthreads();
+    const uint64_t t0 = blockIdx.x * (uint64_t)kRadixTile;
+    for (int k = threadIdx.x; k < kRadixTile; k += kRadixThreads) {
+        uint64_t i = t0 + k;
+        if (i < n) atomicAdd(&h[(keys[i] >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    hist[(uint64_t)threadIdx.x * n_tiles + blockIdx.x] = h[threadIdx.x];
+}
+
+// Stable scatter: thread t owns tile items [16t, 16t+16) in order, so the
+// rank of an item is (items of its digit in earlier threads) + (earlier items
+// of its digit in the same thread).
+__global__ void __launch_bounds__(kRadixThreads) k_radix_scatter(const uint32_t *__restrict__ kin,
+                                                                 const uint32_t *__restrict__ vin, uint64_t n,
+                                                                 int shift, const uint32_t *__restrict__ off,
+                                                                 uint64_t n_tiles, uint32_t *__restrict__ kout,
+                                                                 uint32_t *__restrict__ vout) {
+    extern __shared__ uint16_t sm[];  // [256 threads][256 digits]
+    uint16_t *row = sm + threadIdx.x * 256;
+    for (int d = 0; d < 256; d++) row[d] = 0;
+    const uint64_t i0 = blockIdx.x * (uint64_t)kRadixTile + (uint64_t)threadIdx.x * kRadixItems;
+    uint32_t k[kRadixItems], v[kRadixItems];
+#pragma unroll
+    for (int j = 0; j < kRadixItems; j++) {
+        uint64_t i = i0 + j;
+        k[j] = i < n ? kin[i] : 0u;
+        v[j] = i < n ? vin[i] : 0u;
+        if (i < n) row[(k[j] >> shift) & 255u]++;
+    }
+    __syncthreads();
+    {  // thread d: exclusive scan of digit d over threads
+        const int d = threadIdx.x;
+        uint32_t run = 0;
+        for (int t = 0; t < kRadixThreads; t++) {
+            uint16_t c = sm[t * 256 + d];
+            sm[t * 256 + d] = (uint16_t)run;
+            run += c;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kRadixItems; j++) {
+        uint64_t i = i0 + j;
+        if (i < n) {
+            uint32_t d = (k[j] >> shift) & 255u;
+            uint64_t dst = (uint64_t)off[(uint64_t)d * n_tiles + blockIdx.x] + row[d];
+            row[d]++;
+            kout[dst] = k[j];
+            vout[dst] = v[j];
+        }
+    }
+}
+
+// idx[h] = number of sorted keys <= h.
+__global__ void k_bucket_ends(const uint32_t *__restrict__ keys, uint64_t n, uint64_t n_buckets,
+                              uint32_t *__restrict__ idx) {
+    for (uint64_t h = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; h < n_buckets;
+         h += (uint64_t)gridDim.x * blockDim.x) {
+        uint64_t lo = 0, hi = n;
+        while (lo < hi) {
+            uint64_t mid = (lo + hi) >> 1;
+            if (keys[mid] <= h) lo = mid + 1; else hi = mid;
+        }
+        idx[h] = (uint32_t)lo;
+    }
+}
+
+unsigned grid_for(uint64_t n, int threads, unsigned cap = 152u * 32u) {
+    uint64_t g = (n + threads - 1) / threads;
+    if (g < 1) g = 1;
+    return (unsigned)(g > cap ? cap : g);
+}
+
+}  // namespace
+
+uint64_t packed_words(uint64_t len) {
+    uint64_t w = (len + 2 * (uint64_t)kPadBases + 7) / 8;
+    return (w + 3) & ~3ull;  // whole 16-byte vectors
+}
+
+cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, uint32_t *d_packed, uint64_t words,
+                        cudaStream_t st) {
+    k_pack<<<grid_for(words, 256), 256, 0, st>>>(d_codes, len, with_parity, d_packed, words); count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedShape &sh, const uint32_t *d_idx,
+                         uint32_t *d_cnt, uint32_t *d_lo, uint64_t *d_block_sum, cudaStream_t st) {
+    uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
+    if (!nb) return cudaSuccess;
+    k_count<<<(unsigned)nb, kCountBlock, 0, st>>>(d_query, n_seeds, sh, d_idx, d_cnt, d_lo, d_block_sum); count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, uint64_t *d_incl, uint64_t *d_total,
+                            cudaStream_t st) {
+    k_scan<uint64_t, uint64_t><<<1, 1024, 0, st>>>(d_in, n, d_excl, d_incl, d_total); count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prefix(const uint32_t *d_cnt, uint64_t n_seeds, const uint64_t *d_block_excl, uint32_t *d_P,
+                          cudaStream_t st) {
+    uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
+    if (!nb) return cudaSuccess;
+    k_prefix<<<(unsigned)nb, kCountBlock, 0, st>>>(d_cnt, n_seeds, d_block_excl, d_P); count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expand(const uint32_t *d_P, const uint32_t *d_cnt, const uint32_t *d_lo, const uint32_t *d_pos,
+                          const hspz_chunk &c, int span, int dense, hspz_anchor *d_out, cudaStream_t st) {
+    uint64_t ns = (uint64_t)c.seed_end - c.seed_begin;
+    if (!ns || c.hit_end == c.hit_begin) return cudaSuccess;
+    uint2 *out = reinterpret_cast<uint2 *>(d_out);
+    if (dense) {
+        uint64_t threads = ns * 32;
+        k_expand_dense<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(d_P, d_cnt, d_lo, d_pos, c.seed_begin,
+                                                                          c.seed_end, c.hit_begin, span, out); count_launch();
+    } else {
+        k_expand_sparse<<<(unsigned)((ns + 255) / 256), 256, 0, st>>>(d_P, d_cnt, d_lo, d_pos, c.seed_begin,
+                                                                      c.seed_end, c.hit_begin, span, out); count_launch();
+    }
+    return cudaGetLastError();
+}
+
+// Reference index on the device.  Temporary buffers come from the stream's
+// memory pool and are released before return.
+cudaError_t build_index_tables(const uint8_t *d_ref, uint64_t ref_len, const SeedShape &sh, uint32_t *d_idx,
+                               uint32_t **d_pos_out, uint64_t *n_pos_out, cudaStream_t st) {
+    cudaError_t e;
+    const uint64_t n_buckets = 1ull << (2 * sh.weight);
+    const uint64_t n_win = ref_len >= (uint64_t)sh.span ? ref_len - sh.span + 1 : 0;
+    *d_pos_out = nullptr;
+    *n_pos_out = 0;
+    if (n_win == 0) {
+        return cudaMemsetAsync(d_idx, 0, n_buckets * 4, st);
+    }
+    uint8_t *flags = nullptr;
+    uint32_t *starts = nullptr, *scratch = nullptr, *k0 = nullptr, *v0 = nullptr, *k1 = nullptr, *v1 = nullptr,
+             *hist = nullptr;
+    uint64_t *d_n = nullptr;
+    uint64_t n = 0;
+    const uint64_t n_tiles_max = (n_win + kRadixTile - 1) / kRadixTile;
+#define TRY(x)                        \
+    do {                              \
+        e = (x);                      \
+        if (e != cudaSuccess) goto out; \
+    } while (0)
+    TRY(cudaMallocAsync((void **)&flags, n_win, st));
+    TRY(cudaMallocAsync((void **)&starts, n_win * 4, st));
+    TRY(cudaMallocAsync((void **)&scratch, compact_scratch_words(n_win) * 4, st));
+    TRY(cudaMallocAsync((void **)&d_n, 8, st));
+    k_window_flags<<<grid_for(n_win, 256), 256, 0, st>>>(d_ref, n_win, sh, flags); count_launch();
+    TRY(cudaGetLastError());
+    TRY(launch_compact(flags, n_win, 0, starts, n_win, scratch, d_n, st));
+    TRY(cudaMemcpyAsync(&n, d_n, 8, cudaMemcpyDeviceToHost, st));
+    TRY(cudaStreamSynchronize(st));
+    if (n) {
+        const uint64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
+        (void)n_tiles_max;
+        TRY(cudaMallocAsync((void **)&k0, n * 4, st));
+        TRY(cudaMallocAsync((void **)&v0, n * 4, st));
+        TRY(cudaMallocAsync((void **)&k1, n * 4, st));
+        TRY(cudaMallocAsync((void **)&v1, n * 4, st));
+        TRY(cudaMallocAsync((void **)&hist, n_tiles * 256 * 4, st));
+        k_window_keys<<<grid_for(n, 256), 256, 0, st>>>(d_ref, starts, n, sh, k0, v0); count_launch();
+        TRY(cudaGetLastError());
+        const int smem = kRadixThreads * 256 * 2;
+        TRY(cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, smem));
+        for (int shift = 0; shift < 2 * sh.weight; shift += 8) {
+            k_radix_hist<<<(unsigned)n_tiles, kRadixThreads, 0, st>>>(k0, n, shift, hist, n_tiles); count_launch();
+            TRY(cudaGetLastError());
+            k_scan<uint32_t, uint32_t><<<1, 1024, 0, st>>>(hist, n_tiles * 256, hist, nullptr, nullptr); count_launch();
+            TRY(cudaGetLastError());
+            k_radix_scatter<<<(unsigned)n_tiles, kRadixThreads, smem, st>>>(k0, v0, n, shift, hist, n_tiles, k1, v1); count_launch();
+            TRY(cudaGetLastError());
+            uint32_t *t = k0; k0 = k1; k1 = t;
+            t = v0; v0 = v1; v1 = t;
+        }
+        k_bucket_ends<<<grid_for(n_buckets, 256), 256, 0, st>>>(k0, n, n_buckets, d_idx); count_launch();
+        TRY(cudaGetLastError());
+        TRY(cudaMalloc((void **)d_pos_out, n * 4));
+        TRY(cudaMemcpyAsync(*d_pos_out, v0, n * 4, cudaMemcpyDeviceToDevice, st));
+    } else {
+        TRY(cudaMemsetAsync(d_idx, 0, n_buckets * 4, st));
+    }
+    *n_pos_out = n;
+out:
+#undef TRY
+    for (void *p : {(void *)flags, (void *)starts, (void *)scratch, (void *)k0, (void *)v0, (void *)k1, (void *)v1,
+                    (void *)hist, (void *)d_n})
+        if (p) cudaFreeAsync(p, st);
+    cudaError_t e2 = cudaStreamSynchronize(st);
+    return e != cudaSuccess ? e : e2;
+}
+
+}  // namespace hspz

@@ -1,0 +1,114 @@
+// Internal definitions shared by the CUDA translation units of libhspz.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "hspz.h"
+
+namespace hspz {
+
+// Packed sequences hold 8 bases per uint32 (one nibble each, base i of a word
+// in bits 4i..4i+3) behind kPadBases bases of padding at both ends, so window
+// loads around any in-range anchor stay inside the buffer.
+//   reference nibble: bits 0-1 code, bit 2 = code0 ^ code1 (1 for C and G), bit 3 = N
+//   query nibble:     bits 0-1 code, bit 2 = 0,                              bit 3 = N
+// An N keeps code bits 0.  Padding nibbles are N.
+constexpr int kPadBases = 128;
+constexpr int kPadWords = kPadBases / 8;
+constexpr uint32_t kNibN = 0x8u;
+constexpr int kMaxSpan = 32;
+constexpr int kMaxWeight = 12;
+constexpr int kCountBlock = 256;  // seeds per count/scan block (C.2: 256 counts per block)
+
+struct SeedShape {
+    int span;
+    int weight;
+    int care[kMaxSpan];
+};
+
+struct ScoreArgs {
+    int32_t m[25];
+    int32_t xdrop;
+    int32_t T;
+    // complement-symmetric int8 table for the fast gate: entry (r ^ q) | parity(r) << 2
+    uint32_t tab_lo, tab_hi;
+    int fast;  // 1 when the fast table reproduces m exactly on A/C/G/T
+};
+
+struct SeqView {
+    const uint32_t *packed;  // padded packed words
+    uint64_t len;            // bases
+};
+
+int parse_pattern(const char *pat, SeedShape *sh);
+int make_score_args(const hspz_score_params *p, ScoreArgs *out);
+uint64_t packed_words(uint64_t len);
+
+// kernel launch accounting (every launch site calls count_launch(k) for k launches)
+void count_launch(uint64_t k = 1);
+
+// error plumbing
+void set_error(const std::string &msg);
+int cuda_fail(cudaError_t e, const char *what);
+#define HSPZ_CUDA(call)                                          \
+    do {                                                         \
+        cudaError_t e_ = (call);                                 \
+        if (e_ != cudaSuccess) return hspz::cuda_fail(e_, #call); \
+    } while (0)
+
+// launchers (each returns cudaError_t of the launch)
+cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, uint32_t *d_packed, uint64_t words,
+                        cudaStream_t st);
+cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedShape &sh, const uint32_t *d_idx,
+                         uint32_t *d_cnt, uint32_t *d_lo, uint64_t *d_block_sum, cudaStream_t st);
+cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, uint64_t *d_incl,
+                            uint64_t *d_total, cudaStream_t st);
+cudaError_t launch_prefix(const uint32_t *d_cnt, uint64_t n_seeds, const uint64_t *d_block_excl, uint32_t *d_P,
+                          cudaStream_t st);
+cudaError_t launch_expand(const uint32_t *d_P, const uint32_t *d_cnt, const uint32_t *d_lo, const uint32_t *d_pos,
+                          const hspz_chunk &c, int span, int dense, hspz_anchor *d_out, cudaStream_t st);
+cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const uint32_t *d_pos,
+                               const hspz_chunk &c, int span, SeqView ref, SeqView qry, const ScoreArgs &sa,
+                               hspz_anchor *d_out, uint8_t *d_flags, cudaStream_t st);
+cudaError_t launch_gate(const hspz_anchor *d_anchors, uint64_t n, SeqView ref, SeqView qry, const ScoreArgs &sa,
+                        uint8_t *d_flags, cudaStream_t st);
+cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
+                               uint64_t n_ids, SeqView ref, SeqView qry, const ScoreArgs &sa,
+                               hspz_segment_pair *d_out, uint8_t *d_done, cudaStream_t st);
+// stable compaction in three launches; d_scratch holds compact_scratch_words(n) uint32
+uint64_t compact_scratch_words(uint64_t n);
+cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
+                           uint32_t *d_scratch, uint64_t *d_total, cudaStream_t st);
+
+}  // namespace hspz
+
+struct hspz_index {
+    hspz::SeedShape shape;
+    uint64_t ref_len;
+    uint64_t n_pos;
+    uint32_t *d_idx;  // 4^weight inclusive bucket ends
+    uint32_t *d_pos;  // n_pos reference ends grouped by bucket
+    uint32_t *d_ref;  // packed reference
+    uint64_t ref_words;
+    int device;
+};
+
+struct hspz_plan {
+    const hspz_index *index;
+    uint64_t query_len;
+    uint64_t n_seeds;
+    uint64_t total;
+    uint32_t *d_P;          // inclusive prefix, n_seeds
+    uint32_t *d_lo;         // bucket start per seed
+    uint32_t *d_cnt;        // hit count per seed
+    uint64_t *d_blk;        // per 256-seed block: sums, exclusive and inclusive prefixes, total (3*nb + 1)
+    uint64_t n_blocks;
+    uint32_t *d_qry;        // packed query
+    uint64_t qry_words;
+    std::vector<hspz_chunk> chunks;
+    uint64_t max_chunk_hits;
+};

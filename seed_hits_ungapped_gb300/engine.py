@@ -1,0 +1,127 @@
+"""One query batch through the whole path, as a sequence of C-ABI calls.
+
+``HspEngine`` owns a reference index and reusable device buffers; ``run``
+takes one query batch (a CUDA uint8 tensor) and, per MAX_HITS chunk, calls
+hspz_expand_gate -> hspz_compact -> hspz_materialize -> hspz_compact (accepted).
+Every step runs in libhspz; this module only allocates torch buffers and
+passes pointers.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import List, Optional
+
+import numpy as np
+
+from . import hspz
+
+
+@dataclasses.dataclass
+class ChunkResult:
+    hit_begin: int
+    n_anchors: int
+    n_survivors: int
+    n_accepted: int
+    anchors: Optional[np.ndarray] = None   # (n, 2) uint32, when kept
+    flags: Optional[np.ndarray] = None     # (n,) uint8
+    ids: Optional[np.ndarray] = None       # (n_survivors,) uint32 global anchor ids
+    records: Optional[np.ndarray] = None   # (n_survivors, 4) int32 SegmentPairs
+    done: Optional[np.ndarray] = None      # (n_survivors,) uint8
+    accepted: Optional[np.ndarray] = None  # (n_accepted,) uint32 indices into the survivor list
+
+
+@dataclasses.dataclass
+class BatchResult:
+    n_seeds: int
+    total_hits: int
+    chunks: np.ndarray
+    per_chunk: List[ChunkResult]
+    prefix: Optional[np.ndarray] = None
+
+    @property
+    def n_survivors(self):
+        return sum(c.n_survivors for c in self.per_chunk)
+
+    @property
+    def n_accepted(self):
+        return sum(c.n_accepted for c in self.per_chunk)
+
+
+def _np_u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+class HspEngine:
+    """Reference index + scoring parameters + device buffers for repeated batches."""
+
+    def __init__(self, ref, matrix, xdrop: int, K: int, pattern: str = hspz.DEFAULT_PATTERN, stream=None):
+        import torch
+        self.torch = torch
+        if not torch.cuda.is_available():
+            raise RuntimeError("HspEngine needs a CUDA device (the path has no CPU implementation)")
+        d_ref = ref if isinstance(ref, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(ref, np.uint8))
+        d_ref = d_ref.to(device="cuda", dtype=torch.uint8).contiguous()
+        self.stream = stream
+        self.index = hspz.hspz_build_index(d_ref, pattern, stream=stream)
+        self.ref_len = d_ref.numel()
+        self.params = hspz.score_params(matrix, xdrop, K)
+        self.T = hspz.hspz_keep_threshold(K)
+        self._bufs = {}
+
+    def buffer(self, name: str, n: int, dtype, cols: int = 1):
+        """A reusable device buffer with room for n rows (grown geometrically)."""
+        torch = self.torch
+        have = self._bufs.get(name)
+        if have is None or have.shape[0] < n:
+            rows = max(n, int(1.25 * have.shape[0]) if have is not None else n, 1)
+            shape = (rows, cols) if cols > 1 else (rows,)
+            if have is not None:
+                del self._bufs[name]
+                del have
+            self._bufs[name] = torch.empty(shape, dtype=dtype, device="cuda")
+        return self._bufs[name]
+
+    def _compact(self, flags, n, id_base, name):
+        torch = self.torch
+        ids = self.buffer(name, max(1, n // 64), torch.int32)
+        try:
+            return ids, hspz.hspz_compact(flags, n, id_base, ids, stream=self.stream)
+        except hspz.HspzError as e:
+            if e.status != hspz.HSPZ_E_CAPACITY:
+                raise
+            ids = self.buffer(name, e.needed, torch.int32)
+            return ids, hspz.hspz_compact(flags, n, id_base, ids, stream=self.stream)
+
+    def plan(self, d_query, max_hits: int = 0, walk_full: bool = False):
+        return hspz.hspz_find_hits(self.index, d_query, max_hits, walk_full, stream=self.stream)
+
+    def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False) -> BatchResult:
+        torch = self.torch
+        plan = self.plan(d_query, max_hits, walk_full)
+        out = []
+        for c in range(plan.n_chunks):
+            hb, he = int(plan.chunks[c, 2]), int(plan.chunks[c, 3])
+            n = he - hb
+            anchors = self.buffer("anchors", n, torch.int32, 2)
+            flags = self.buffer("flags", n, torch.uint8)
+            hspz.hspz_expand_gate(plan, c, self.params, anchors, flags, stream=self.stream)
+            ids, n_surv = self._compact(flags, n, hb, "ids")
+            rec = self.buffer("records", n_surv, torch.int32, 4)
+            done = self.buffer("done", n_surv, torch.uint8)
+            hspz.hspz_materialize(self.index, plan, anchors, hb, ids, n_surv, self.params, rec, done,
+                                  stream=self.stream)
+            acc, n_acc = self._compact(done, n_surv, 0, "accepted")
+            r = ChunkResult(hb, n, n_surv, n_acc)
+            if keep:
+                r.anchors = _np_u32(anchors[:n]).reshape(-1, 2).copy()
+                r.flags = flags[:n].cpu().numpy().copy()
+                r.ids = _np_u32(ids[:n_surv]).copy()
+                r.records = rec[:n_surv].cpu().numpy().copy()
+                r.done = done[:n_surv].cpu().numpy().copy()
+                r.accepted = _np_u32(acc[:n_acc]).copy()
+            out.append(r)
+        res = BatchResult(plan.n_seeds, plan.total_hits, plan.chunks.copy(), out)
+        if keep:
+            res.prefix = _np_u32(plan.prefix())
+        plan.close()
+        return res

@@ -28,7 +28,8 @@ count in proportion for oracle-sized parity cases):
             frozen workload A (hg38 x mm39 unit 0), which is not available.
   chunking  workload_a plus a 4,000 bp poly-A run written into the reference
             and copied into the query; both query strands (forward and reverse
-            complement) as separate batches; hit cap 2^24.
+            complement) as separate batches; hit cap 2^24.  (Scaled cases shrink
+            the poly-A run with the lengths and the cap with the anchor count.)
 
 Scoring for every workload: HOXD70 (A/C/G/T block) with N scoring -100 against
 anything, X-drop 910, hsp threshold K = 3000.
@@ -188,7 +189,7 @@ def make(name: str, scale: float = 1.0) -> Workload:
     qry = _background(rng, _sz(25_000_000, scale), GC41)
     occ = None
     if name == "chunking":
-        ln = 4000
+        ln = 4000 if scale == 1.0 else max(40, int(round(4000 * scale)))
         p = int(rng.integers(0, ref.size - ln + 1))
         ref[p:p + ln] = A
         dst = int(rng.integers(0, qry.size - ln + 1))
@@ -198,7 +199,7 @@ def make(name: str, scale: float = 1.0) -> Workload:
     _plant(rng, ref, qry, _sz(10_000, scale), 100, 3000, 0.05, 0.25, occ)
     if name == "workload_a":
         return Workload(name, ref, [qry], m, seed=seed, scale=scale)
-    cap = max(1, int(round((1 << 24) * scale)))
+    cap = max(1, int(round((1 << 24) * scale * scale)))  # anchors grow with both lengths
     return Workload(name, ref, [qry, reverse_complement(qry)], m, max_hits=cap, seed=seed, scale=scale)
 
 

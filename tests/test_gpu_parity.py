@@ -1,0 +1,246 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Integer work throughout, so every comparison is bit-exact: prefix, chunk list,
+anchors, flags, survivor ids, SegmentPairs, done flags and accepted ids.
+Oracle-sized cases are compared element by element; the full-size workload in
+the benchmark's launch configuration is compared on the full prefix and on
+sampled anchors, flags and records computed one by one by the oracle.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from seed_hits_ungapped_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    from seed_hits_ungapped_gb300 import hspz
+    hspz.load_library()  # fails loudly when the library is missing
+    return torch
+
+
+def _engine(torch_cuda, ref, matrix, xdrop, K, pattern=oracle.SEED_PATTERN):
+    from seed_hits_ungapped_gb300.engine import HspEngine
+    return HspEngine(ref, matrix, xdrop, K, pattern=pattern)
+
+
+def _dev(torch, a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
+
+
+def assert_same_as_oracle(gpu, orc):
+    assert orc["rc"] == 0
+    assert gpu.total_hits == orc["total"]
+    assert np.array_equal(gpu.prefix, orc["P"])
+    assert np.array_equal(gpu.chunks, orc["chunks"])
+    assert len(gpu.per_chunk) == len(orc["per_chunk"])
+    for g, o in zip(gpu.per_chunk, orc["per_chunk"]):
+        assert np.array_equal(g.anchors, o["anchors"])
+        assert np.array_equal(g.flags, o["flags"])
+        assert np.array_equal(g.ids, o["ids"])
+        assert np.array_equal(g.records, o["rec"])
+        assert np.array_equal(g.done, o["done"])
+        assert np.array_equal(g.accepted, o["accepted"])
+
+
+def run_both(torch, ref, qry, matrix, xdrop, K, max_hits=0, pattern=oracle.SEED_PATTERN, walk_full=False):
+    eng = _engine(torch, ref, matrix, xdrop, K, pattern)
+    gpu = eng.run(_dev(torch, qry), max_hits=max_hits, walk_full=walk_full, keep=True)
+    orc = oracle.run_path(ref, qry, matrix, xdrop, K, max_hits=max_hits, pattern=pattern)
+    return gpu, orc
+
+
+# ------------------------------------------------------------------ worked example
+
+def test_worked_example_on_gpu(torch_cuda):
+    """Counts 0 3 1 0 5 from the figure of "C. Hit discovery": a one-base seed
+    over reference CCCGTTTTT and query ACGNT puts 0, 3, 1, 0 and 5 reference
+    occurrences behind seeds 0..4."""
+    from seed_hits_ungapped_gb300 import hspz
+    rows, slots = {}, {}
+    for line in open(os.path.join(HERE, "golden", "hit_discovery_worked_example.txt")):
+        line = line.strip()
+        if line and not line.startswith("#"):
+            k, *v = line.split()
+            v = [int(x) for x in v]
+            if k == "slots":
+                slots[v[0]] = v[1:]
+            else:
+                rows[k] = v
+    ref = np.array([1, 1, 1, 2, 3, 3, 3, 3, 3], np.uint8)
+    qry = np.array([0, 1, 2, 4, 3], np.uint8)
+    torch = torch_cuda
+    index = hspz.hspz_build_index(_dev(torch, ref), "1")
+    plan = hspz.hspz_find_hits(index, _dev(torch, qry))
+    P = plan.prefix().cpu().numpy().view(np.uint32)
+    assert P.tolist() == rows["prefix"]
+    assert plan.total_hits == 9 and plan.chunks.tolist() == [[0, 5, 0, 9]]
+    for mode in (hspz.HSPZ_EXPAND_SPARSE, hspz.HSPZ_EXPAND_DENSE, hspz.HSPZ_EXPAND_AUTO):
+        a = torch.full((9, 2), -1, dtype=torch.int32, device="cuda")
+        hspz.hspz_expand(plan, 0, a, mode)
+        a = a.cpu().numpy()
+        bucket_start = {1: 0, 2: 3, 4: 4}  # reference position of occurrence j = 0
+        for s, want in slots.items():
+            for j, slot in enumerate(want):
+                assert a[slot].tolist() == [bucket_start[s] + j, s]
+
+
+# ------------------------------------------------------------------ element-wise parity
+
+def test_tiny_full_size(torch_cuda):
+    w = synth.make("tiny")
+    gpu, orc = run_both(torch_cuda, w.ref, w.query, w.matrix, w.xdrop, w.K)
+    assert gpu.total_hits > 30_000 and gpu.n_survivors > 10_000
+    assert_same_as_oracle(gpu, orc)
+
+
+@pytest.mark.parametrize("name,scale", [("mid", 0.1), ("dense", 0.03), ("workload_a", 0.02), ("chunking", 0.02)])
+def test_scaled_workloads(torch_cuda, name, scale):
+    w = synth.make(name, scale=scale)
+    for qry in w.queries:
+        gpu, orc = run_both(torch_cuda, w.ref, qry, w.matrix, w.xdrop, w.K, max_hits=w.max_hits)
+        assert_same_as_oracle(gpu, orc)
+        if name == "chunking":
+            assert len(gpu.chunks) > 3
+
+
+def test_chunk_walk_modes_agree(torch_cuda):
+    w = synth.make("chunking", scale=0.02)
+    a, orc = run_both(torch_cuda, w.ref, w.query, w.matrix, w.xdrop, w.K, max_hits=w.max_hits, walk_full=True)
+    assert_same_as_oracle(a, orc)
+
+
+@pytest.mark.parametrize("xdrop,K", [(0, 1), (50, 200), (910, 3000), (1 << 30, 5000)])
+def test_general_matrix(torch_cuda, xdrop, K):
+    """An asymmetric random matrix (not complement-symmetric) and extreme X/K."""
+    rng = np.random.default_rng(xdrop + K)
+    m = rng.integers(-150, 120, (5, 5)).astype(np.int32)
+    m[np.arange(4), np.arange(4)] = rng.integers(60, 130, 4)
+    w = synth.make("tiny", scale=0.2)
+    gpu, orc = run_both(torch_cuda, w.ref, w.query, m, xdrop, K)
+    assert_same_as_oracle(gpu, orc)
+
+
+def test_edges(torch_cuda):
+    rng = np.random.default_rng(11)
+    m = synth.hoxd70()
+    s = rng.integers(0, 4, 5000).astype(np.uint8)
+    # identical sequences: every anchor extends to both sequence edges
+    gpu, orc = run_both(torch_cuda, s, s.copy(), m, 910, 3000)
+    assert_same_as_oracle(gpu, orc)
+    assert any((g.records[:, 0] == 0).any() for g in gpu.per_chunk)
+    # query with N everywhere, a query shorter than the seed, an N-rich reference
+    for qry in (np.full(400, 4, np.uint8), s[:18].copy(), s[:19].copy()):
+        gpu, orc = run_both(torch_cuda, s, qry, m, 910, 3000)
+        assert_same_as_oracle(gpu, orc)
+    ref = s.copy()
+    ref[rng.random(ref.size) < 0.2] = 4
+    gpu, orc = run_both(torch_cuda, ref, s[1000:3000].copy(), m, 910, 3000)
+    assert_same_as_oracle(gpu, orc)
+    # a reference shorter than the seed span: an empty index
+    gpu, orc = run_both(torch_cuda, s[:10].copy(), s[:500].copy(), m, 910, 3000)
+    assert gpu.total_hits == 0 and orc["total"] == 0
+
+
+def test_expansion_mappings_and_standalone_gate(torch_cuda):
+    """C.4: sparse and dense mappings give the fused kernel's anchors; the
+    standalone gate over those anchors gives the fused flags."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    w = synth.make("dense", scale=0.03)
+    eng = _engine(torch, w.ref, w.matrix, w.xdrop, w.K)
+    plan = eng.plan(_dev(torch, w.query))
+    n = plan.total_hits
+    assert n > 100_000
+    fused = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+    flags = torch.empty(n, dtype=torch.uint8, device="cuda")
+    hspz.hspz_expand_gate(plan, 0, eng.params, fused, flags)
+    for mode in (hspz.HSPZ_EXPAND_SPARSE, hspz.HSPZ_EXPAND_DENSE, hspz.HSPZ_EXPAND_AUTO):
+        a = torch.full((n, 2), -1, dtype=torch.int32, device="cuda")
+        hspz.hspz_expand(plan, 0, a, mode)
+        assert torch.equal(a, fused)
+    f2 = torch.full((n,), 7, dtype=torch.uint8, device="cuda")
+    hspz.hspz_score_gate(eng.index, plan, fused, n, eng.params, f2)
+    assert torch.equal(f2, flags)
+
+
+def test_compaction_alignment_and_capacity(torch_cuda):
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    rng = np.random.default_rng(5)
+    for n in (1, 15, 16, 17, 4095, 4096, 4097, 100_003):
+        f = (rng.random(n + 3) < 0.3).astype(np.uint8) * rng.integers(1, 256, n + 3).astype(np.uint8)
+        d = torch.from_numpy(f).cuda()
+        for off in (0, 1, 3):
+            view = d[off:off + n]
+            ids = torch.empty(n + 1, dtype=torch.int32, device="cuda")
+            k = hspz.hspz_compact(view, n, 1000, ids)
+            want = oracle.compact(f[off:off + n], 1000)
+            assert k == want.size
+            assert np.array_equal(ids[:k].cpu().numpy().view(np.uint32), want)
+    # too small: nothing written, the needed count is reported
+    f = np.ones(100, np.uint8)
+    ids = torch.full((10,), -7, dtype=torch.int32, device="cuda")
+    with pytest.raises(hspz.HspzError) as e:
+        hspz.hspz_compact(torch.from_numpy(f).cuda(), 100, 0, ids)
+    assert e.value.needed == 100
+    assert (ids.cpu().numpy() == -7).all()
+
+
+def test_refusal_edge_on_gpu(torch_cuda):
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    ref = np.zeros(65_554, np.uint8)
+    index = hspz.hspz_build_index(_dev(torch, ref))
+    with pytest.raises(hspz.HspzError) as e:
+        hspz.hspz_find_hits(index, _dev(torch, np.zeros(65_554, np.uint8)))
+    assert e.value.status == hspz.HSPZ_E_HIT_OVERFLOW and e.value.total_hits == 1 << 32
+    qry = np.zeros(65_553, np.uint8)
+    cap = 1 << 30
+    plan = hspz.hspz_find_hits(index, _dev(torch, qry), max_hits=cap)
+    assert plan.total_hits == (1 << 32) - 65_536
+    idx, pos = oracle.build_index(ref)
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, oracle.seed_buckets(qry)))
+    assert np.array_equal(plan.chunks, oracle.chunk_walk(P, cap))
+    assert np.array_equal(plan.prefix().cpu().numpy().view(np.uint32), P)
+
+
+# ------------------------------------------------------------------ full size, sampled
+
+@pytest.mark.slow
+def test_workload_a_full_size_sampled(torch_cuda):
+    """The benchmark workload at full size, in the benchmark's launch
+    configuration: full prefix, sampled anchors and flags, every survivor's
+    flag, sampled records."""
+    torch = torch_cuda
+    w = synth.make("workload_a")
+    eng = _engine(torch, w.ref, w.matrix, w.xdrop, w.K)
+    gpu = eng.run(_dev(torch, w.query), keep=True)
+    idx, pos = oracle.build_index(w.ref)
+    buckets = oracle.seed_buckets(w.query)
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
+    assert rc == 0 and gpu.total_hits == total
+    assert np.array_equal(gpu.prefix, P)
+    assert np.array_equal(gpu.chunks, oracle.chunk_walk(P, 0))
+    ch = gpu.per_chunk[0]
+    rng = np.random.default_rng(0)
+    sample = np.unique(rng.integers(0, total, 20_000))
+    want = oracle.anchors_at(idx, pos, buckets, P, sample)
+    assert np.array_equal(ch.anchors[sample], want)
+    assert np.array_equal(ch.flags[sample], oracle.gate(w.ref, w.query, want, w.matrix, w.xdrop, eng.T))
+    # every survivor really passes, and survivors are exactly the set flags
+    assert np.array_equal(ch.ids, np.flatnonzero(ch.flags).astype(np.uint32))
+    assert oracle.gate(w.ref, w.query, ch.anchors[ch.ids], w.matrix, w.xdrop, eng.T).all()
+    pick = np.unique(rng.integers(0, ch.ids.size, 5_000))
+    rec, done = oracle.materialize(w.ref, w.query, ch.anchors, 0, ch.ids[pick], w.matrix, w.xdrop, eng.T)
+    assert np.array_equal(ch.records[pick], rec) and np.array_equal(ch.done[pick], done)
