@@ -184,10 +184,10 @@ class Index:
 
 
 class _DeviceView:
-    """Read-only view of a library-owned device buffer for torch.as_tensor."""
+    """View of a library-owned device buffer for torch.as_tensor (copied at once)."""
 
     def __init__(self, ptr: int, n: int, typestr: str = "<i4"):
-        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, True), "version": 2}
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": typestr, "data": (ptr, False), "version": 2}
 
 
 def _copy_device(ptr: int, n: int):
