@@ -196,6 +196,26 @@ int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t 
                  uint64_t *n_out, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * hspz_compact without any device allocation.  The hspZ pages have no
+ * counterpart to this call; it exists for callers that cannot allocate device
+ * memory while they run -- a program whose device memory was handed in full
+ * to another allocator at start-up, so cudaMalloc would fail, or one that
+ * must not take the implicit device synchronization cudaMalloc/cudaFree can
+ * cause.  Same arguments, result and statuses as hspz_compact, for at most
+ * hspz_compact_noalloc_max_flags() = 2^28 flags (larger n: HSPZ_E_INVAL with
+ * a message in hspz_last_error).  Its scratch is one fixed device array of
+ * about 768 KiB inside the library, held by every GPU that loads the library
+ * until the process exits.  The first call on a device looks up that array's
+ * device address (once per device, with the device current); make that first
+ * call before any stream capture.  All calls share the one array, so calls
+ * that overlap on the GPU (different streams or threads at the same time)
+ * race and must be serialized by the caller.  Synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_compact_noalloc(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
+                         uint64_t *n_out, void *stream);
+uint64_t hspz_compact_noalloc_max_flags(void);
+
+/* ------------------------------------------------------------------------ *
  * Exact X-drop materialization ("E. X-drop materialization", E.1-E.5).  For
  * survivor k with global id d_ids[k], the anchor d_anchors[d_ids[k] - id_base]
  * (n_anchors entries; an id outside [id_base, id_base + n_anchors) yields a

@@ -33,7 +33,8 @@ EXPORTS = [
     "hspz_strerror", "hspz_last_error", "hspz_abi_version", "hspz_keep_threshold", "hspz_build_index",
     "hspz_index_free", "hspz_index_info", "hspz_index_tables", "hspz_find_hits", "hspz_plan_free",
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
-    "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host",
+    "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
+    "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags",
 ]
 
 
@@ -88,6 +89,9 @@ def load_library():
         "hspz_compact": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_materialize": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
         "hspz_chunk_walk_host": (ctypes.c_int, [VP, U64, U64, ctypes.c_int, P(hspz_chunk), U32, P(U32)]),
+        "hspz_kernel_launches": (U64, []),
+        "hspz_compact_noalloc": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
+        "hspz_compact_noalloc_max_flags": (U64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -297,6 +301,25 @@ def hspz_compact(d_flags, n: int, id_base: int, d_ids, stream=None) -> int:
         err.needed = out.value
         raise err
     _check(rc, "hspz_compact")
+    return out.value
+
+
+def hspz_compact_noalloc(d_flags, n: int, id_base: int, d_ids, stream=None) -> int:
+    """hspz_compact for callers that cannot allocate device memory: the scratch
+    is a fixed array inside the library (at most 2^28 flags per call; calls
+    that overlap on the GPU share that array and must be serialized)."""
+    import torch
+    if d_flags.numel() < n:
+        raise ValueError("flags shorter than n")
+    out = ctypes.c_uint64(0)
+    rc = load_library().hspz_compact_noalloc(_dptr(d_flags, torch.uint8, "d_flags"), int(n), int(id_base),
+                                             _dptr(d_ids, torch.int32, "d_ids"), d_ids.numel(), ctypes.byref(out),
+                                             _stream(stream))
+    if rc == HSPZ_E_CAPACITY:
+        err = HspzError(rc, "hspz_compact_noalloc", "needs %d ids" % out.value)
+        err.needed = out.value
+        raise err
+    _check(rc, "hspz_compact_noalloc")
     return out.value
 
 

@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert len(names) >= 19
     for n in names:
         assert hasattr(lib, n), n
-    assert sorted(hspz.EXPORTS + ["hspz_kernel_launches"]) == names or set(hspz.EXPORTS) <= set(names)
+    assert sorted(hspz.EXPORTS) == names
     assert lib.hspz_abi_version() == 1
 
 
