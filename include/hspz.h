@@ -168,6 +168,8 @@ int hspz_expand(const hspz_plan *plan, uint32_t chunk, int mode, hspz_anchor *d_
 /* ------------------------------------------------------------------------ *
  * Fused expansion + score gate of one chunk (C.5 + D.1-D.3): writes the same
  * anchors as hspz_expand and, for each, the flag byte of hspz_score_gate.
+ * Uses a small tile table owned by the plan, so two hspz_expand_gate calls on
+ * one plan must not run at the same time on the GPU.
  * ------------------------------------------------------------------------ */
 int hspz_expand_gate(const hspz_plan *plan, uint32_t chunk, const hspz_score_params *params,
                      hspz_anchor *d_anchors, uint8_t *d_flags, uint64_t cap, void *stream);

@@ -198,7 +198,9 @@ int hspz_build_index(const uint8_t *d_ref, uint64_t ref_len, const char *seed_pa
     ix->ref_words = packed_words(ref_len);
     cudaError_t e = cudaMalloc((void **)&ix->d_idx, nb * 4);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref, ix->ref_words * 4);
-    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, ix->d_ref, ix->ref_words, st);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref_rev, ix->ref_words * 4);
+    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 0, ix->d_ref, ix->ref_words, st);
+    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 1, ix->d_ref_rev, ix->ref_words, st);
     if (e == cudaSuccess) e = build_index_tables(d_ref, ref_len, sh, ix->d_idx, &ix->d_pos, &ix->n_pos, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) {
@@ -215,6 +217,7 @@ void hspz_index_free(hspz_index *ix) {
     if (ix->d_idx) cudaFree(ix->d_idx);
     if (ix->d_pos) cudaFree(ix->d_pos);
     if (ix->d_ref) cudaFree(ix->d_ref);
+    if (ix->d_ref_rev) cudaFree(ix->d_ref_rev);
     delete ix;
 }
 
@@ -235,7 +238,8 @@ int hspz_index_tables(const hspz_index *ix, const uint32_t **d_idx, const uint32
 
 void hspz_plan_free(hspz_plan *p) {
     if (!p) return;
-    for (void *q : {(void *)p->d_P, (void *)p->d_lo, (void *)p->d_cnt, (void *)p->d_blk, (void *)p->d_qry})
+    for (void *q : {(void *)p->d_P, (void *)p->d_lo, (void *)p->d_cnt, (void *)p->d_blk, (void *)p->d_qry,
+                    (void *)p->d_qry_rev, (void *)p->d_tiles})
         if (q) cudaFree(q);
     delete p;
 }
@@ -262,7 +266,9 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_cnt, sa * 4);
     if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_blk, (3 * nb + 1) * 8);
     if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_qry, p->qry_words * 4);
-    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, p->d_qry, p->qry_words, st);
+    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_qry_rev, p->qry_words * 4);
+    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 0, p->d_qry, p->qry_words, st);
+    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 1, p->d_qry_rev, p->qry_words, st);
     uint64_t *bsum = p->d_blk, *bexcl = p->d_blk + nb, *bincl = p->d_blk + 2 * nb, *dtot = p->d_blk + 3 * nb;
     if (e == cudaSuccess && S) e = launch_count(d_query, S, ix->shape, ix->d_idx, p->d_cnt, p->d_lo, bsum, st);
     if (e == cudaSuccess && S) e = launch_scan_u64(bsum, nb, bexcl, bincl, dtot, st);
@@ -319,6 +325,12 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     p->max_chunk_hits = 0;
     for (const auto &c : p->chunks)
         p->max_chunk_hits = std::max<uint64_t>(p->max_chunk_hits, (uint64_t)c.hit_end - c.hit_begin);
+    e = cudaMalloc((void **)&p->d_tiles, expand_gate_tile_words(p->max_chunk_hits) * 4);
+    if (e != cudaSuccess) {
+        rc = cuda_fail(e, "hspz_find_hits tile scratch");
+        hspz_plan_free(p);
+        return rc;
+    }
     *plan_out = p;
     return HSPZ_OK;
 }
@@ -373,9 +385,9 @@ int hspz_expand_gate(const hspz_plan *p, uint32_t chunk, const hspz_score_params
     const uint64_t hits = (uint64_t)c.hit_end - c.hit_begin;
     if (cap < hits) return HSPZ_E_CAPACITY;
     if (hits && (!d_anchors || !d_flags)) return HSPZ_E_INVAL;
-    SeqView r{p->index->d_ref, p->index->ref_len}, q{p->d_qry, p->query_len};
+    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
     cudaError_t e = launch_expand_gate(p->d_P, p->d_lo, p->index->d_pos, c, p->index->shape.span, r, q, sa,
-                                       d_anchors, d_flags, (cudaStream_t)stream);
+                                       d_anchors, d_flags, p->d_tiles, (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_expand_gate");
 }
 
@@ -384,7 +396,7 @@ int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor 
     if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags))) return HSPZ_E_INVAL;
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
-    SeqView r{ix->d_ref, ix->ref_len}, q{p->d_qry, p->query_len};
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
     cudaError_t e = launch_gate(d_anchors, n, r, q, sa, d_flags, (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate");
 }
@@ -420,7 +432,7 @@ int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor
     if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
-    SeqView r{ix->d_ref, ix->ref_len}, q{p->d_qry, p->query_len};
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
     cudaError_t e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done,
                                        (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize");

@@ -56,6 +56,131 @@ __device__ __forceinline__ int gate_one(const Seqs &s, const int *__restrict__ t
     return 0;
 }
 
+// ------------------------------------------------------------------ fast gate
+// For matrices that are complement symmetric on A/C/G/T (score(r, q) =
+// score(r ^ 3, q ^ 3) with A0 C1 G2 T3) and fit int8, the score of a base pair
+// depends only on x = r ^ q and the reference base's strong/weak class
+// (bit 2 of the reference nibble), so eight pairs are scored by two byte
+// permutes of one 8-entry table.  A walk advances eight bases per step:
+// the eight running sums come from byte dot products, a step that cannot hold
+// the stop (its lowest running sum is not more than X below the highest
+// maximum it could reach) just takes the new maximum, and only a step that
+// might hold the stop is replayed base by base.  N anywhere in a step's
+// sixteen nibbles sends that step to the 5 x 5 matrix.
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Scores of one 8-base step, in walk order, as 8 int32 running sums from S.
+// RIGHT: walk order = nibbles 0..7 of the aligned words; left: 7..0.
+template <bool RIGHT>
+__device__ __forceinline__ void step_sums(uint32_t R, uint32_t Q, uint32_t keep, uint32_t tlo, uint32_t thi,
+                                          const int *__restrict__ tab25, int S, int (&Sv)[8]) {
+    const uint32_t nmask = (R | Q) & 0x88888888u & keep;
+    if (__builtin_expect(nmask == 0, 1)) {
+        // masked-off nibbles select entry 0 in sign mode: score 0
+        const uint32_t idx = (((R ^ Q) & 0x77777777u) & keep) | (0x88888888u & ~keep);
+        const uint32_t w0 = prmt(tlo, thi, idx), w1 = prmt(tlo, thi, idx >> 16);
+        const uint32_t a = RIGHT ? w0 : w1, b = RIGHT ? w1 : w0;
+        const int c1 = RIGHT ? 0x00000001 : 0x01000000, c2 = RIGHT ? 0x00000101 : 0x01010000;
+        const int c3 = RIGHT ? 0x00010101 : 0x01010100, c4 = 0x01010101;
+        Sv[0] = __dp4a((int)a, c1, S);
+        Sv[1] = __dp4a((int)a, c2, S);
+        Sv[2] = __dp4a((int)a, c3, S);
+        Sv[3] = __dp4a((int)a, c4, S);
+        Sv[4] = __dp4a((int)b, c1, Sv[3]);
+        Sv[5] = __dp4a((int)b, c2, Sv[3]);
+        Sv[6] = __dp4a((int)b, c3, Sv[3]);
+        Sv[7] = __dp4a((int)b, c4, Sv[3]);
+    } else {
+        int run = S;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const int nib = RIGHT ? k : 7 - k;
+            const uint32_t kb = (keep >> (4 * nib)) & 0xFu;
+            const uint32_t rn = (R >> (4 * nib)) & 0xFu, qn = (Q >> (4 * nib)) & 0xFu;
+            const uint32_t rc = (rn & 8u) ? 4u : (rn & 3u), qc = (qn & 8u) ? 4u : (qn & 3u);
+            run += kb ? tab25[rc * 5 + qc] : 0;
+            Sv[k] = run;
+        }
+    }
+}
+
+// One side of the X-drop walk.  Returns the side maximum before the stop
+// (or the maximum at which the walk already reached `need`, with *accepted).
+template <bool RIGHT>
+__device__ __forceinline__ int walk_fast(const uint32_t *__restrict__ ref, const uint32_t *__restrict__ qry,
+                                         uint32_t ar, uint32_t aq, uint32_t limit, uint32_t tlo, uint32_t thi,
+                                         const int *__restrict__ tab25, int X, int need, bool *accepted) {
+    int S = 0, M = 0;
+    if (limit == 0) return 0;
+    // nibble index (with padding) of the lowest base of the first step
+    const uint32_t jr = (RIGHT ? ar : ar - 8u) + (uint32_t)kPadBases;
+    const uint32_t jq = (RIGHT ? aq : aq - 8u) + (uint32_t)kPadBases;
+    const uint32_t shr = (jr & 7u) * 4u, shq = (jq & 7u) * 4u;
+    const uint32_t *pr = ref + (jr >> 3), *pq = qry + (jq >> 3);
+    uint32_t r0 = __ldg(pr), r1 = __ldg(pr + 1), q0 = __ldg(pq), q1 = __ldg(pq + 1);
+    uint32_t rem = limit;
+    for (;;) {
+        const uint32_t R = __funnelshift_r(r0, r1, shr);
+        const uint32_t Q = __funnelshift_r(q0, q1, shq);
+        uint32_t keep = 0xFFFFFFFFu;
+        if (rem < 8) keep = RIGHT ? ((1u << (4 * rem)) - 1u) : ~((1u << (4 * (8 - rem))) - 1u);
+        int Sv[8];
+        step_sums<RIGHT>(R, Q, keep, tlo, thi, tab25, S, Sv);
+        const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
+        const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
+        const int Mb = max(M, hi);
+        if (lo < Mb - X) {  // the stop may lie in this step: replay it base by base
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                if (M - Sv[k] > X) {
+                    *accepted = M >= need;
+                    return M;
+                }
+                M = max(M, Sv[k]);
+            }
+        }
+        M = Mb;
+        if (M >= need) {
+            *accepted = true;
+            return M;
+        }
+        if (rem <= 8) return M;
+        rem -= 8;
+        S = Sv[7];
+        if (RIGHT) {
+            r0 = r1;
+            q0 = q1;
+            pr++;
+            pq++;
+            r1 = __ldg(pr + 1);
+            q1 = __ldg(pq + 1);
+        } else {
+            r1 = r0;
+            q1 = q0;
+            pr--;
+            pq--;
+            r0 = __ldg(pr);
+            q0 = __ldg(pq);
+        }
+    }
+}
+
+__device__ __forceinline__ int gate_fast(const Seqs &s, const int *__restrict__ tab25, uint32_t tlo, uint32_t thi,
+                                         int X, int T, uint32_t ar, uint32_t aq) {
+    if (ar >= s.Lr || aq >= s.Lq) return 0;
+    bool acc = false;
+    const int ML = walk_fast<false>(s.ref, s.qry, ar, aq, min(ar, aq), tlo, thi, tab25, X, T, &acc);
+    if (acc) return 1;
+    const uint32_t nr = (uint32_t)min(s.Lr - ar, s.Lq - aq);
+    walk_fast<true>(s.ref, s.qry, ar, aq, nr, tlo, thi, tab25, X, T - ML, &acc);
+    return acc ? 1 : 0;
+}
+
 __device__ __forceinline__ uint32_t upper_bound_g(const uint32_t *__restrict__ P, uint32_t lo, uint32_t hi,
                                                   uint32_t key) {
     while (lo < hi) {
@@ -74,7 +199,7 @@ constexpr int kFuseSeeds = 2048;
 // chunk.  Each slot's seed is the first seed whose inclusive prefix exceeds
 // the slot's global id; its occurrence index follows from the backward slot
 // rule j = P[s] - 1 - id.  The anchor is written, then gated.
-template <bool GATE>
+template <bool GATE, bool FAST>
 __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__restrict__ P,
                                                               const uint32_t *__restrict__ lo,
                                                               const uint32_t *__restrict__ pos, uint32_t sb,
@@ -120,10 +245,282 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
         const uint32_t j = pend - 1 - gid;
         const uint32_t re = __ldg(pos + __ldg(lo + s) + j), qe = s + span - 1;
         out[t] = make_uint2(re, qe);
-        if (GATE) flags[t] = (uint8_t)gate_one(sq, tab, sa.xdrop, sa.T, re, qe);
+        if (GATE) {
+            const int keep = FAST ? gate_fast(sq, tab, sa.tab_lo, sa.tab_hi, sa.xdrop, sa.T, re, qe)
+                                  : gate_one(sq, tab, sa.xdrop, sa.T, re, qe);
+            flags[t] = (uint8_t)keep;
+        }
     }
 }
 
+// ------------------------------------------------------------------ warp helpers for the fused fast kernel
+constexpr unsigned kFullMask = 0xFFFFFFFFu;
+
+// First s in [lo, hi) with P[s] > key (hi if none); called by a whole warp.
+__device__ __forceinline__ uint32_t warp_upper_bound(const uint32_t *__restrict__ P, uint32_t lo, uint32_t hi,
+                                                     uint32_t key, int lane) {
+    while (hi - lo > 31) {
+        const uint32_t span = hi - lo;
+        const uint32_t probe = lo + (uint32_t)(((uint64_t)span * (uint32_t)(lane + 1)) / 33u);
+        const unsigned m = __ballot_sync(kFullMask, __ldg(P + probe) > key);
+        const int f = m ? __ffs(m) - 1 : 32;
+        const uint32_t below = __shfl_sync(kFullMask, probe, f > 0 ? f - 1 : 0);
+        const uint32_t above = __shfl_sync(kFullMask, probe, f < 32 ? f : 31);
+        const uint32_t nlo = f == 0 ? lo : below + 1;
+        const uint32_t nhi = f == 32 ? hi : above;
+        lo = nlo;
+        hi = nhi;
+    }
+    const uint32_t idx = lo + (uint32_t)lane;
+    const unsigned m = __ballot_sync(kFullMask, idx >= hi || __ldg(P + idx) > key);
+    return lo + (uint32_t)(__ffs(m) - 1);
+}
+
+struct WalkState {
+    const uint32_t *pr, *pq;
+    uint32_t shr, shq, r0, r1, q0, q1, rem;
+    int S, M;
+};
+
+// Where one side of anchor (ar, aq) starts: word pointers, shifts and length.
+__device__ __forceinline__ void walk_place(WalkState &w, const Seqs &sq, const uint32_t *ref_rev,
+                                           const uint32_t *qry_rev, uint32_t ar, uint32_t aq, int side) {
+    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
+    const uint32_t rb = side ? ar : Lr - ar;
+    const uint32_t qb = side ? aq : Lq - aq;
+    w.rem = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
+    const uint32_t jr = rb + (uint32_t)kPadBases, jq = qb + (uint32_t)kPadBases;
+    w.pr = (side ? sq.ref : ref_rev) + (jr >> 3);
+    w.pq = (side ? sq.qry : qry_rev) + (jq >> 3);
+    w.shr = (jr & 7u) * 4u;
+    w.shq = (jq & 7u) * 4u;
+    w.S = 0;
+    w.M = 0;
+}
+
+// Start one side of anchor (ar, aq): side 0 walks left (forward over the
+// reversed sequences from the base before the anchor), side 1 walks right.
+__device__ __forceinline__ void walk_start(WalkState &w, const Seqs &sq, const uint32_t *ref_rev,
+                                           const uint32_t *qry_rev, uint32_t ar, uint32_t aq, int side) {
+    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
+    const uint32_t rb = side ? ar : Lr - ar;
+    const uint32_t qb = side ? aq : Lq - aq;
+    w.rem = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
+    const uint32_t jr = rb + (uint32_t)kPadBases, jq = qb + (uint32_t)kPadBases;
+    w.pr = (side ? sq.ref : ref_rev) + (jr >> 3);
+    w.pq = (side ? sq.qry : qry_rev) + (jq >> 3);
+    w.shr = (jr & 7u) * 4u;
+    w.shq = (jq & 7u) * 4u;
+    w.r0 = __ldg(w.pr);
+    w.r1 = __ldg(w.pr + 1);
+    w.q0 = __ldg(w.pq);
+    w.q1 = __ldg(w.pq + 1);
+    w.S = 0;
+    w.M = 0;
+}
+
+__device__ __forceinline__ void walk_advance(WalkState &w, int S_next) {
+    w.rem -= 8;
+    w.S = S_next;
+    w.r0 = w.r1;
+    w.q0 = w.q1;
+    w.pr++;
+    w.pq++;
+    w.r1 = __ldg(w.pr + 1);
+    w.q1 = __ldg(w.pq + 1);
+}
+
+// The common 8-base step.  It advances the walk and returns false unless the
+// step may hold the stop, reaches `need` or ends at the edge; then it leaves
+// the walk untouched and returns true for walk_resolve.
+__device__ __forceinline__ bool walk_step(WalkState &w, uint32_t tlo, uint32_t thi, const int *__restrict__ tab25,
+                                          int X, int need, int (&Sv)[8], int &Mb, bool &maybe_stop) {
+    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
+    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
+    const uint32_t keep = w.rem >= 8 ? 0xFFFFFFFFu : ((1u << (4 * w.rem)) - 1u);
+    step_sums<true>(R, Q, keep, tlo, thi, tab25, w.S, Sv);
+    const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
+    const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
+    Mb = max(w.M, hi);
+    maybe_stop = lo < Mb - X;
+    if (!(maybe_stop | (Mb >= need) | (w.rem <= 8))) {
+        w.M = Mb;
+        walk_advance(w, Sv[7]);
+        return false;
+    }
+    return true;
+}
+
+// Settles a flagged step.  Returns true when the side is over, with *acc
+// telling whether its maximum reached `need`; else the walk has advanced.
+__device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], int Mb, bool maybe_stop, int X,
+                                             int need, bool *acc) {
+    if (maybe_stop) {
+        int M = w.M;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            if (M - Sv[k] > X) {
+                w.M = M;
+                *acc = M >= need;
+                return true;
+            }
+            M = max(M, Sv[k]);
+        }
+    }
+    w.M = Mb;
+    if (Mb >= need) {
+        *acc = true;
+        return true;
+    }
+    if (w.rem <= 8) {
+        *acc = false;
+        return true;
+    }
+    walk_advance(w, Sv[7]);
+    return false;
+}
+
+constexpr int kWWarps = 8;             // warps per CTA
+constexpr int kWUnit = 256;            // anchor slots per warp
+constexpr int kWTile = kWWarps * kWUnit;
+constexpr int kWSeeds = 2048;          // cached seed prefixes per CTA
+
+// The seeds of the first and last anchor slot of every tile (thread per tile).
+__global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
+                             uint64_t n_tiles, uint32_t *__restrict__ tiles) {
+    for (uint64_t t = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; t < n_tiles;
+         t += (uint64_t)gridDim.x * blockDim.x) {
+        const uint64_t s0 = t * kWTile, s1 = min(n_hits, s0 + kWTile) - 1;
+        const uint32_t a = upper_bound_g(P, sb, se, hb + (uint32_t)s0);
+        tiles[2 * t] = a;
+        tiles[2 * t + 1] = upper_bound_g(P, a, se, hb + (uint32_t)s1);
+    }
+}
+
+// Fused expansion + gate.  The CTA owns kWTile consecutive anchor slots and
+// caches the prefixes of the seeds they come from; after that one barrier
+// every warp works alone on its own 256 slots:
+//   1. lane l expands slots 8l..8l+7 of the warp's share into shared memory
+//      (search for the first slot's seed, then walk forward);
+//   2. the gate runs in 8 synchronous rounds of 32 anchors (one per lane):
+//      all lanes start their left side together, step until every lane has
+//      flagged a step that may hold its stop, reaches `need` or ends at the
+//      edge, settle together, then the same for the right side;
+//   3. the warp stores its anchors and flags with coalesced writes.
+__global__ void __launch_bounds__(kWWarps * 32, 5)
+    k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
+                    const uint32_t *__restrict__ pos, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
+                    uint32_t span, Seqs sq, const uint32_t *__restrict__ ref_rev,
+                    const uint32_t *__restrict__ qry_rev, const uint32_t *__restrict__ tiles, ScoreArgs sa,
+                    uint2 *__restrict__ out, uint8_t *__restrict__ flags) {
+    __shared__ uint2 sA_all[kWTile];
+    __shared__ uint32_t sP[kWSeeds];
+    __shared__ int tab[25];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint64_t tile0 = (uint64_t)blockIdx.x * kWTile;
+    const uint32_t tile_count = (uint32_t)min((uint64_t)kWTile, n_hits - tile0);
+    if (tid < 25) tab[tid] = sa.m[tid];
+    const uint32_t first = __ldg(tiles + 2 * (uint64_t)blockIdx.x), ns = __ldg(tiles + 2 * (uint64_t)blockIdx.x + 1) - first + 1;
+    const bool cached = ns <= (uint32_t)kWSeeds;
+    if (cached)
+        for (uint32_t i = tid; i < ns; i += kWWarps * 32) sP[i] = __ldg(P + first + i);
+    __syncthreads();
+    const uint32_t wbase = (uint32_t)warp * kWUnit;  // this warp's slots within the tile
+    if (wbase >= tile_count) return;
+    const uint32_t count = min((uint32_t)kWUnit, tile_count - wbase);
+    const uint64_t t0 = tile0 + wbase;
+    uint2 *sA = sA_all + wbase;
+
+    // 1. expansion
+    const uint32_t i0 = (uint32_t)lane * 8u;
+    if (i0 < count) {
+        const uint32_t g0 = hb + (uint32_t)t0 + i0;
+        uint32_t l;
+        if (cached) {
+            uint32_t x = 0, y = ns;
+            while (x < y) {
+                const uint32_t mid = (x + y) >> 1;
+                if (sP[mid] <= g0) x = mid + 1; else y = mid;
+            }
+            l = x;
+        } else {
+            l = upper_bound_g(P, first, first + ns, g0) - first;
+        }
+        uint32_t pend = cached ? sP[l] : __ldg(P + first + l);
+        uint32_t base = __ldg(lo + first + l);
+        const uint32_t kmax = min(8u, count - i0);
+        for (uint32_t k = 0; k < kmax; k++) {
+            const uint32_t g = g0 + k;
+            while (pend <= g) {
+                l++;
+                pend = cached ? sP[l] : __ldg(P + first + l);
+                base = __ldg(lo + first + l);
+            }
+            sA[i0 + k] = make_uint2(__ldg(pos + base + (pend - 1 - g)), first + l + span - 1);
+        }
+    }
+    __syncwarp();
+
+    // 2. gate rounds
+    const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
+    const int X = sa.xdrop, T = sa.T;
+    for (uint32_t round = 0; round * 32 < count; round++) {
+        const uint32_t ai = round * 32u + (uint32_t)lane;
+        const bool valid = ai < count;
+        uint2 a = make_uint2(0, 0);
+        if (valid) a = sA[ai];
+        bool accepted = false;
+        int need = T;
+        uint32_t nr0 = 0, nr1 = 0, nq0 = 0, nq1 = 0;  // the right side's first words
+#pragma unroll 1
+        for (int side = 0; side < 2; side++) {
+            const bool walk = valid && !accepted;
+            WalkState w;
+            if (walk) {
+                walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
+                if (side == 0) {  // the left side's first words, and the right side's, in one go
+                    w.r0 = __ldg(w.pr);
+                    w.r1 = __ldg(w.pr + 1);
+                    w.q0 = __ldg(w.pq);
+                    w.q1 = __ldg(w.pq + 1);
+                    const uint32_t jr = a.x + (uint32_t)kPadBases, jq = a.y + (uint32_t)kPadBases;
+                    nr0 = __ldg(sq.ref + (jr >> 3));
+                    nr1 = __ldg(sq.ref + (jr >> 3) + 1);
+                    nq0 = __ldg(sq.qry + (jq >> 3));
+                    nq1 = __ldg(sq.qry + (jq >> 3) + 1);
+                } else {
+                    w.r0 = nr0;
+                    w.r1 = nr1;
+                    w.q0 = nq0;
+                    w.q1 = nq1;
+                }
+            }
+            bool ended = !walk, stepping = walk;
+            int Sv[8], Mb = 0;
+            bool maybe_stop = false;
+            while (__any_sync(kFullMask, !ended)) {
+                while (__any_sync(kFullMask, stepping)) {
+                    if (stepping && walk_step(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+                }
+                if (!ended) {
+                    bool acc = false;
+                    if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
+                        ended = true;
+                        accepted = acc;
+                        if (side == 0) need = T - w.M;
+                    } else {
+                        stepping = true;
+                    }
+                }
+            }
+        }
+        if (valid) flags[t0 + ai] = accepted ? 1 : 0;
+    }
+    // 3. anchors
+    for (uint32_t i = lane; i < count; i += 32) out[t0 + i] = sA[i];
+}
+
+template <bool FAST>
 __global__ void __launch_bounds__(256) k_gate(const uint2 *__restrict__ anchors, uint64_t n, Seqs sq, ScoreArgs sa,
                                               uint8_t *__restrict__ flags) {
     __shared__ int tab[25];
@@ -131,7 +528,8 @@ __global__ void __launch_bounds__(256) k_gate(const uint2 *__restrict__ anchors,
     __syncthreads();
     for (uint64_t i = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; i < n; i += (uint64_t)gridDim.x * blockDim.x) {
         const uint2 a = anchors[i];
-        flags[i] = (uint8_t)gate_one(sq, tab, sa.xdrop, sa.T, a.x, a.y);
+        flags[i] = (uint8_t)(FAST ? gate_fast(sq, tab, sa.tab_lo, sa.tab_hi, sa.xdrop, sa.T, a.x, a.y)
+                                  : gate_one(sq, tab, sa.xdrop, sa.T, a.x, a.y));
     }
 }
 
@@ -153,7 +551,241 @@ __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict_
     best_n = nb;
 }
 
+// Exact side walk in 8-base steps with the earliest maximum (E.2/E.3), for
+// the complement-symmetric int8 matrices of the fast gate.  Sums stay in
+// int32 because the caller routes walks longer than 2^24 bases to
+// side_exact.
+template <bool RIGHT>
+__device__ __forceinline__ void walk_exact_fast(const uint32_t *__restrict__ ref, const uint32_t *__restrict__ qry,
+                                                uint32_t ar, uint32_t aq, uint32_t limit, uint32_t tlo,
+                                                uint32_t thi, const int *__restrict__ tab25, int X, int64_t &best,
+                                                uint64_t &best_n) {
+    int S = 0, M = 0;
+    uint32_t nb = 0, base = 0;
+    best = 0;
+    best_n = 0;
+    if (limit == 0) return;
+    const uint32_t jr = (RIGHT ? ar : ar - 8u) + (uint32_t)kPadBases;
+    const uint32_t jq = (RIGHT ? aq : aq - 8u) + (uint32_t)kPadBases;
+    const uint32_t shr = (jr & 7u) * 4u, shq = (jq & 7u) * 4u;
+    const uint32_t *pr = ref + (jr >> 3), *pq = qry + (jq >> 3);
+    uint32_t r0 = __ldg(pr), r1 = __ldg(pr + 1), q0 = __ldg(pq), q1 = __ldg(pq + 1);
+    uint32_t rem = limit;
+    for (;;) {
+        const uint32_t R = __funnelshift_r(r0, r1, shr);
+        const uint32_t Q = __funnelshift_r(q0, q1, shq);
+        uint32_t keep = 0xFFFFFFFFu;
+        if (rem < 8) keep = RIGHT ? ((1u << (4 * rem)) - 1u) : ~((1u << (4 * (8 - rem))) - 1u);
+        int Sv[8];
+        step_sums<RIGHT>(R, Q, keep, tlo, thi, tab25, S, Sv);
+        const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
+        const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
+        if (lo < max(M, hi) - X) {
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                if (M - Sv[k] > X) {
+                    best = M;
+                    best_n = nb;
+                    return;
+                }
+                if (Sv[k] > M) {
+                    M = Sv[k];
+                    nb = base + k + 1;
+                }
+            }
+        } else if (hi > M) {
+            int k = 7;
+#pragma unroll
+            for (int i = 6; i >= 0; i--)
+                if (Sv[i] == hi) k = i;
+            M = hi;
+            nb = base + k + 1;
+        }
+        if (rem <= 8) break;
+        rem -= 8;
+        base += 8;
+        S = Sv[7];
+        if (RIGHT) {
+            r0 = r1;
+            q0 = q1;
+            pr++;
+            pq++;
+            r1 = __ldg(pr + 1);
+            q1 = __ldg(pq + 1);
+        } else {
+            r1 = r0;
+            q1 = q0;
+            pr--;
+            pq--;
+            r0 = __ldg(pr);
+            q0 = __ldg(pq);
+        }
+    }
+    best = M;
+    best_n = nb;
+}
+
+// ------------------------------------------------------------------ warp materializer
+// One warp per survivor (E.1-E.5), in tiles of 256 bases: lane l holds the
+// 8 walk steps 8l+1..8l+8 of the tile.  The lanes' running sums come from
+// byte dot products plus a warp exclusive scan of the lane sums; the maximum
+// before each lane from an exclusive max-scan; each lane tests its own steps
+// for a drop against that maximum and a ballot picks the first dropping lane
+// (E.2: "ballot the first lane beyond X-drop").  The earliest step attaining
+// the side maximum is found by a second ballot (E.2 invariant).  Left walks
+// run forward over the reversed sequences.
+
+__device__ __forceinline__ int warp_excl_sum(int v, int lane, int *total) {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, x, o);
+        if (lane >= o) x += y;
+    }
+    *total = __shfl_sync(kFullMask, x, 31);
+    return x - v;
+}
+
+__device__ __forceinline__ int warp_excl_max(int v, int lane, int init, int *all) {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFullMask, x, o);
+        if (lane >= o) x = max(x, y);
+    }
+    *all = max(init, __shfl_sync(kFullMask, x, 31));
+    const int prev = __shfl_up_sync(kFullMask, x, 1);
+    return lane ? max(init, prev) : init;
+}
+
+// One side of survivor anchor (ar, aq); every lane returns the same result.
+// Inside a tile all values are relative to the running sum at the tile start
+// (int32: bounded by X plus one tile of scores); only the absolute running
+// sum and maximum are 64-bit, so walks of any length stay exact.
+__device__ __forceinline__ void warp_side(const Seqs &sq, const uint32_t *ref_rev, const uint32_t *qry_rev,
+                                          uint32_t ar, uint32_t aq, int side, uint32_t tlo, uint32_t thi,
+                                          const int *__restrict__ tab25, int X, int lane, int64_t &best,
+                                          uint32_t &best_n) {
+    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
+    const uint32_t rb = side ? ar : Lr - ar, qb = side ? aq : Lq - aq;
+    const uint32_t limit = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
+    const uint32_t jr = rb + (uint32_t)kPadBases, jq = qb + (uint32_t)kPadBases;
+    const uint32_t *wr = (side ? sq.ref : ref_rev) + (jr >> 3);
+    const uint32_t *wq = (side ? sq.qry : qry_rev) + (jq >> 3);
+    const uint32_t shr = (jr & 7u) * 4u, shq = (jq & 7u) * 4u;
+    int64_t St = 0, Mt = 0;
+    int Dt = 0;  // Mt - St, never above X while the walk goes on
+    uint32_t nb = 0;
+    for (uint32_t base0 = 0; base0 < limit; base0 += 256) {
+        const uint32_t off = base0 / 8 + (uint32_t)lane;
+        const uint32_t R = __funnelshift_r(__ldg(wr + off), __ldg(wr + off + 1), shr);
+        const uint32_t Q = __funnelshift_r(__ldg(wq + off), __ldg(wq + off + 1), shq);
+        const uint32_t first = base0 + 8u * (uint32_t)lane;  // steps before this lane's first
+        const uint32_t valid = limit > first ? min(limit - first, 8u) : 0u;
+        const uint32_t keep = valid >= 8 ? 0xFFFFFFFFu : ((1u << (4 * valid)) - 1u);
+        int L[8];
+        step_sums<true>(R, Q, keep, tlo, thi, tab25, 0, L);
+        int tot;
+        const int E = warp_excl_sum(L[7], lane, &tot);  // lane start, relative to the tile start
+        int lm = L[0];
+#pragma unroll
+        for (int k = 1; k < 8; k++) lm = max(lm, L[k]);
+        int pm_all;
+        const int PM = warp_excl_max(E + lm, lane, Dt, &pm_all);  // maximum before this lane (relative)
+        int kd = 8;  // first step of this lane that drops (8: none)
+        int ll = L[0];
+#pragma unroll
+        for (int k = 1; k < 8; k++) ll = min(ll, L[k]);
+        if (ll < max(PM - E, lm) - X) {  // a drop is possible in this lane: find it
+            int rk = PM - E;             // running maximum relative to this lane's start
+#pragma unroll
+            for (int k = 0; k < 8; k++) {
+                if (kd == 8 && rk - L[k] > X) kd = k;
+                rk = max(rk, L[k]);
+            }
+        }
+        const unsigned dm = __ballot_sync(kFullMask, kd < 8);
+        int Mnew;
+        int cut = 8;  // steps of this lane inside the walk
+        if (dm) {
+            const int f = __ffs(dm) - 1;
+            int mine = PM;
+#pragma unroll
+            for (int k = 0; k < 8; k++)
+                if (k < kd) mine = max(mine, E + L[k]);
+            Mnew = __shfl_sync(kFullMask, mine, f);
+            cut = lane < f ? 8 : (lane == f ? kd : 0);
+        } else {
+            Mnew = pm_all;
+        }
+        if (Mnew > Dt) {  // earliest step reaching the new maximum: its lane first, then the step
+            bool has = false;
+            if (cut == 8) has = E + lm == Mnew;
+            else if (cut > 0) {
+#pragma unroll
+                for (int k = 0; k < 8; k++)
+                    if (k < cut && E + L[k] == Mnew) has = true;
+            }
+            const unsigned fm = __ballot_sync(kFullMask, has);
+            const int fl = __ffs(fm) - 1;
+            int kf = 0;
+            if (lane == fl) {
+                kf = 7;
+#pragma unroll
+                for (int k = 6; k >= 0; k--)
+                    if (E + L[k] == Mnew) kf = k;
+            }
+            const int kk = __shfl_sync(kFullMask, kf, fl);
+            nb = base0 + 8u * (uint32_t)fl + (uint32_t)kk + 1u;
+            Mt = St + Mnew;
+        }
+        if (dm) break;
+        St += tot;
+        Dt = (int)(Mt - St);
+    }
+    best = Mt;
+    best_n = nb;
+}
+
+__global__ void __launch_bounds__(256) k_materialize_warp(const uint2 *__restrict__ anchors, uint64_t n_anchors,
+                                                          uint32_t id_base, const uint32_t *__restrict__ ids,
+                                                          uint64_t n_ids, Seqs sq,
+                                                          const uint32_t *__restrict__ ref_rev,
+                                                          const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
+                                                          uint4 *__restrict__ out, uint8_t *__restrict__ done) {
+    __shared__ int tab[25];
+    if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
+    for (uint64_t k = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32; k < n_ids; k += warps) {
+        const uint32_t id = ids[k];
+        const uint64_t slot = (uint64_t)id - id_base;
+        const uint2 a = (id >= id_base && slot < n_anchors) ? anchors[slot] : make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+        uint4 rec = make_uint4(0, 0, 0, 0);
+        uint8_t ok = 0;
+        if (a.x < sq.Lr && a.y < sq.Lq) {
+            int64_t ML, MR;
+            uint32_t nL, nR;
+            warp_side(sq, ref_rev, qry_rev, a.x, a.y, 0, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, lane, ML, nL);
+            warp_side(sq, ref_rev, qry_rev, a.x, a.y, 1, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, lane, MR, nR);
+            int64_t score = ML + MR;
+            if (score > 2147483647LL) score = 2147483647LL;
+            if (score >= sa.T) {
+                rec = make_uint4(a.x - (uint32_t)nL, a.y - (uint32_t)nL, (uint32_t)(nL + nR - 1),
+                                 (uint32_t)(int32_t)score);
+                ok = 1;
+            }
+        }
+        if (lane == 0) {
+            out[k] = rec;
+            done[k] = ok;
+        }
+    }
+}
+
 // One thread per survivor (E.1-E.5).
+template <bool FAST>
 __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ anchors, uint64_t n_anchors, uint32_t id_base,
                                                      const uint32_t *__restrict__ ids, uint64_t n_ids, Seqs sq,
                                                      ScoreArgs sa, uint4 *__restrict__ out,
@@ -171,8 +803,15 @@ __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ a
         if (a.x < sq.Lr && a.y < sq.Lq) {
             int64_t ML, MR;
             uint64_t nL, nR;
-            side_exact(sq, tab, sa.xdrop, a.x, a.y, false, ML, nL);
-            side_exact(sq, tab, sa.xdrop, a.x, a.y, true, MR, nR);
+            const uint32_t lim_l = min(a.x, a.y);
+            const uint32_t lim_r = (uint32_t)min(sq.Lr - a.x, sq.Lq - a.y);
+            if (FAST && lim_l < (1u << 24) && lim_r < (1u << 24)) {
+                walk_exact_fast<false>(sq.ref, sq.qry, a.x, a.y, lim_l, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, ML, nL);
+                walk_exact_fast<true>(sq.ref, sq.qry, a.x, a.y, lim_r, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, MR, nR);
+            } else {
+                side_exact(sq, tab, sa.xdrop, a.x, a.y, false, ML, nL);
+                side_exact(sq, tab, sa.xdrop, a.x, a.y, true, MR, nR);
+            }
             int64_t score = ML + MR;
             if (score > 2147483647LL) score = 2147483647LL;
             if (score >= sa.T) {
@@ -195,21 +834,27 @@ Seqs seqs(SeqView r, SeqView q) { return Seqs{r.packed, q.packed, r.len, q.len};
 
 }  // namespace
 
+uint64_t expand_gate_tile_words(uint64_t max_chunk_hits) { return 2 * ((max_chunk_hits + kWTile - 1) / kWTile) + 2; }
+
 cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const uint32_t *d_pos, const hspz_chunk &c,
                                int span, SeqView ref, SeqView qry, const ScoreArgs &sa, hspz_anchor *d_out,
-                               uint8_t *d_flags, cudaStream_t st) {
+                               uint8_t *d_flags, uint32_t *d_tiles, cudaStream_t st) {
     const uint64_t n = (uint64_t)c.hit_end - c.hit_begin;
     if (!n) return cudaSuccess;
     const uint64_t blocks = (n + kFuseTile - 1) / kFuseTile;
     uint2 *out = reinterpret_cast<uint2 *>(d_out);
-    if (d_flags) {
-        k_expand_gate<true><<<(unsigned)blocks, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, c.seed_begin, c.seed_end,
-                                                                       c.hit_begin, n, span, seqs(ref, qry), sa, out,
-                                                                       d_flags); count_launch();
+    const unsigned g = (unsigned)blocks;
+    const uint32_t sb = c.seed_begin, se = c.seed_end, hb = c.hit_begin;
+    if (!d_flags) {
+        k_expand_gate<false, false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
+    } else if (sa.fast) {
+        const uint64_t n_tiles = (n + kWTile - 1) / kWTile;
+        k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
+        k_expand_gate_w<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span,
+                                                                    seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa,
+                                                                    out, d_flags); count_launch();
     } else {
-        k_expand_gate<false><<<(unsigned)blocks, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, c.seed_begin, c.seed_end,
-                                                                        c.hit_begin, n, span, seqs(ref, qry), sa, out,
-                                                                        d_flags); count_launch();
+        k_expand_gate<true, false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     }
     return cudaGetLastError();
 }
@@ -217,8 +862,13 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
 cudaError_t launch_gate(const hspz_anchor *d_anchors, uint64_t n, SeqView ref, SeqView qry, const ScoreArgs &sa,
                         uint8_t *d_flags, cudaStream_t st) {
     if (!n) return cudaSuccess;
-    k_gate<<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
-                                              d_flags); count_launch();
+    if (sa.fast) {
+        k_gate<true><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
+                                                        d_flags); count_launch();
+    } else {
+        k_gate<false><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
+                                                         d_flags); count_launch();
+    }
     return cudaGetLastError();
 }
 
@@ -227,9 +877,17 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
                                SeqView ref, SeqView qry, const ScoreArgs &sa, hspz_segment_pair *d_out,
                                uint8_t *d_done, cudaStream_t st) {
     if (!n_ids) return cudaSuccess;
-    k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n_anchors, id_base, d_ids,
-                                                         n_ids, seqs(ref, qry), sa, reinterpret_cast<uint4 *>(d_out),
-                                                         d_done); count_launch();
+    const uint2 *an = reinterpret_cast<const uint2 *>(d_anchors);
+    uint4 *out = reinterpret_cast<uint4 *>(d_out);
+    if (sa.fast) {
+        const uint64_t warps = n_ids < 152ull * 64 ? n_ids : 152ull * 64;
+        k_materialize_warp<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids,
+                                                                                  seqs(ref, qry), ref.rev, qry.rev, sa,
+                                                                                  out, d_done); count_launch();
+    } else {
+        k_materialize<false><<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry),
+                                                                    sa, out, d_done); count_launch();
+    }
     return cudaGetLastError();
 }
 

@@ -13,11 +13,12 @@ namespace hspz {
 
 // Packed sequences hold 8 bases per uint32 (one nibble each, base i of a word
 // in bits 4i..4i+3) behind kPadBases bases of padding at both ends, so window
-// loads around any in-range anchor stay inside the buffer.
+// loads around any in-range anchor stay inside the buffer: the widest read is
+// a 256-base warp tile plus one word, starting inside the sequence.
 //   reference nibble: bits 0-1 code, bit 2 = code0 ^ code1 (1 for C and G), bit 3 = N
 //   query nibble:     bits 0-1 code, bit 2 = 0,                              bit 3 = N
 // An N keeps code bits 0.  Padding nibbles are N.
-constexpr int kPadBases = 128;
+constexpr int kPadBases = 512;
 constexpr int kPadWords = kPadBases / 8;
 constexpr uint32_t kNibN = 0x8u;
 constexpr int kMaxSpan = 32;
@@ -42,6 +43,7 @@ struct ScoreArgs {
 struct SeqView {
     const uint32_t *packed;  // padded packed words
     uint64_t len;            // bases
+    const uint32_t *rev;     // padded packed words of the reversed sequence (base i = base len-1-i)
 };
 
 int parse_pattern(const char *pat, SeedShape *sh);
@@ -61,8 +63,8 @@ int cuda_fail(cudaError_t e, const char *what);
     } while (0)
 
 // launchers (each returns cudaError_t of the launch)
-cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, uint32_t *d_packed, uint64_t words,
-                        cudaStream_t st);
+cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, int reverse, uint32_t *d_packed,
+                        uint64_t words, cudaStream_t st);
 cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedShape &sh, const uint32_t *d_idx,
                          uint32_t *d_cnt, uint32_t *d_lo, uint64_t *d_block_sum, cudaStream_t st);
 cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, uint64_t *d_incl,
@@ -71,9 +73,11 @@ cudaError_t launch_prefix(const uint32_t *d_cnt, uint64_t n_seeds, const uint64_
                           cudaStream_t st);
 cudaError_t launch_expand(const uint32_t *d_P, const uint32_t *d_cnt, const uint32_t *d_lo, const uint32_t *d_pos,
                           const hspz_chunk &c, int span, int dense, hspz_anchor *d_out, cudaStream_t st);
+// uint32 words of tile scratch the fused kernel needs for a chunk of max_chunk_hits anchors
+uint64_t expand_gate_tile_words(uint64_t max_chunk_hits);
 cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const uint32_t *d_pos,
                                const hspz_chunk &c, int span, SeqView ref, SeqView qry, const ScoreArgs &sa,
-                               hspz_anchor *d_out, uint8_t *d_flags, cudaStream_t st);
+                               hspz_anchor *d_out, uint8_t *d_flags, uint32_t *d_tiles, cudaStream_t st);
 cudaError_t launch_gate(const hspz_anchor *d_anchors, uint64_t n, SeqView ref, SeqView qry, const ScoreArgs &sa,
                         uint8_t *d_flags, cudaStream_t st);
 cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
@@ -92,7 +96,8 @@ struct hspz_index {
     uint64_t n_pos;
     uint32_t *d_idx;  // 4^weight inclusive bucket ends
     uint32_t *d_pos;  // n_pos reference ends grouped by bucket
-    uint32_t *d_ref;  // packed reference
+    uint32_t *d_ref;      // packed reference
+    uint32_t *d_ref_rev;  // packed reversed reference (left walks run forward over it)
     uint64_t ref_words;
     int device;
 };
@@ -108,7 +113,9 @@ struct hspz_plan {
     uint64_t *d_blk;        // per 256-seed block: sums, exclusive and inclusive prefixes, total (3*nb + 1)
     uint64_t n_blocks;
     uint32_t *d_qry;        // packed query
+    uint32_t *d_qry_rev;    // packed reversed query
     uint64_t qry_words;
     std::vector<hspz_chunk> chunks;
     uint64_t max_chunk_hits;
+    uint32_t *d_tiles;      // fused-kernel scratch: first/last seed of every tile of a chunk
 };
