@@ -1,0 +1,107 @@
+"""Full-size parity for every workload, in the launch configuration the
+benchmark uses (the fused expansion + gate, compaction and materializer run
+chunk by chunk through the C ABI).
+
+Integer work throughout, so every compared value is bit-exact.  mid is
+compared element by element.  dense (2.1e9 anchors), workload_a and chunking
+(27 chunks over both strands) are compared on the full prefix and chunk list,
+on anchors, flags and records sampled and recomputed one by one by the oracle,
+and on properties that hold at any size: survivor ids are exactly the set
+flags in increasing order, and every sampled survivor passes the oracle gate.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from seed_hits_ungapped_gb300 import synth
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a CUDA device is required for -m gpu tests")
+    from seed_hits_ungapped_gb300 import hspz
+    hspz.load_library()
+    return torch
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def sampled_parity(torch, w, n_sample=20_000, n_mat=3_000, seed=0):
+    from seed_hits_ungapped_gb300 import hspz
+    from seed_hits_ungapped_gb300.engine import HspEngine
+    rng = np.random.default_rng(seed)
+    eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
+    idx, pos = oracle.build_index(w.ref)
+    checked = 0
+    for qry in w.queries:
+        buckets = oracle.seed_buckets(qry)
+        P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
+        assert rc == 0
+        plan = eng.plan(torch.from_numpy(qry).cuda(), w.max_hits)
+        assert plan.total_hits == total
+        assert np.array_equal(_u32(plan.prefix()), P)
+        assert np.array_equal(plan.chunks, oracle.chunk_walk(P, w.max_hits))
+        for c in range(plan.n_chunks):
+            hb, he = int(plan.chunks[c, 2]), int(plan.chunks[c, 3])
+            n = he - hb
+            anchors = eng.buffer("anchors", n, torch.int32, 2)
+            flags = eng.buffer("flags", n, torch.uint8)
+            hspz.hspz_expand_gate(plan, c, eng.params, anchors, flags)
+            # sampled anchors and flags, one by one by the oracle
+            pick = np.unique(rng.integers(0, n, min(n, n_sample)))
+            pick_t = torch.from_numpy(pick.astype(np.int64)).cuda()
+            got_a = _u32(anchors[pick_t]).reshape(-1, 2)
+            want_a = oracle.anchors_at(idx, pos, buckets, P, pick + hb)
+            assert np.array_equal(got_a, want_a)
+            got_f = flags[pick_t].cpu().numpy()
+            assert np.array_equal(got_f, oracle.gate(w.ref, qry, want_a, w.matrix, w.xdrop, eng.T))
+            # survivors = the set flags, in order (checked on the device)
+            ids, n_surv = eng._compact(flags, n, hb, "ids")
+            want_ids = torch.nonzero(flags[:n]).flatten().to(torch.int64) + hb
+            assert n_surv == want_ids.numel()
+            assert torch.equal(ids[:n_surv].to(torch.int64) & 0xFFFFFFFF, want_ids)
+            if n_surv:
+                rec = eng.buffer("records", n_surv, torch.int32, 4)
+                done = eng.buffer("done", n_surv, torch.uint8)
+                hspz.hspz_materialize(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
+                sp = np.unique(rng.integers(0, n_surv, min(n_surv, n_mat)))
+                sp_t = torch.from_numpy(sp.astype(np.int64)).cuda()
+                sid = _u32(ids[sp_t])
+                sa = oracle.anchors_at(idx, pos, buckets, P, sid)
+                assert oracle.gate(w.ref, qry, sa, w.matrix, w.xdrop, eng.T).all()
+                want_rec, want_done = oracle.materialize(w.ref, qry, sa, 0, np.arange(sp.size, dtype=np.uint32),
+                                                         w.matrix, w.xdrop, eng.T)
+                assert np.array_equal(rec[sp_t].cpu().numpy(), want_rec)
+                assert np.array_equal(done[sp_t].cpu().numpy(), want_done)
+            checked += n
+        plan.close()
+    return checked
+
+
+def test_mid_full_size_elementwise(torch_cuda):
+    from seed_hits_ungapped_gb300.engine import HspEngine
+    w = synth.make("mid")
+    eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
+    gpu = eng.run(torch_cuda.from_numpy(w.query).cuda(), keep=True)
+    orc = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K)
+    assert gpu.total_hits == orc["total"] > 8_000_000
+    assert np.array_equal(gpu.prefix, orc["P"])
+    assert np.array_equal(gpu.chunks, orc["chunks"])
+    for g, o in zip(gpu.per_chunk, orc["per_chunk"]):
+        for a, b in ((g.anchors, o["anchors"]), (g.flags, o["flags"]), (g.ids, o["ids"]),
+                     (g.records, o["rec"]), (g.done, o["done"]), (g.accepted, o["accepted"])):
+            assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("name", ["dense", "workload_a", "chunking"])
+def test_full_size_sampled(torch_cuda, name):
+    w = synth.make(name)
+    checked = sampled_parity(torch_cuda, w)
+    assert checked > 100_000_000
+    torch_cuda.cuda.empty_cache()
