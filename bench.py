@@ -332,6 +332,7 @@ def main():
                    "seeds_per_step": n_seeds, "survivors": res.n_survivors, "accepted": res.n_accepted,
                    "chunks": int(len(res.chunks)), "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "expand_gate_anchors_per_s": n_anchors * args.steps / (sum(gate_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
                      "kernel": "k_expand_gate (fused expansion + score gate)",
