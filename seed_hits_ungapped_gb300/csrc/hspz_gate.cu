@@ -199,7 +199,7 @@ constexpr int kFuseSeeds = 2048;
 // chunk.  Each slot's seed is the first seed whose inclusive prefix exceeds
 // the slot's global id; its occurrence index follows from the backward slot
 // rule j = P[s] - 1 - id.  The anchor is written, then gated.
-template <bool GATE, bool FAST>
+template <bool GATE>
 __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__restrict__ P,
                                                               const uint32_t *__restrict__ lo,
                                                               const uint32_t *__restrict__ pos, uint32_t sb,
@@ -245,11 +245,7 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
         const uint32_t j = pend - 1 - gid;
         const uint32_t re = __ldg(pos + __ldg(lo + s) + j), qe = s + span - 1;
         out[t] = make_uint2(re, qe);
-        if (GATE) {
-            const int keep = FAST ? gate_fast(sq, tab, sa.tab_lo, sa.tab_hi, sa.xdrop, sa.T, re, qe)
-                                  : gate_one(sq, tab, sa.xdrop, sa.T, re, qe);
-            flags[t] = (uint8_t)keep;
-        }
+        if (GATE) flags[t] = (uint8_t)gate_one(sq, tab, sa.xdrop, sa.T, re, qe);
     }
 }
 
@@ -551,241 +547,7 @@ __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict_
     best_n = nb;
 }
 
-// Exact side walk in 8-base steps with the earliest maximum (E.2/E.3), for
-// the complement-symmetric int8 matrices of the fast gate.  Sums stay in
-// int32 because the caller routes walks longer than 2^24 bases to
-// side_exact.
-template <bool RIGHT>
-__device__ __forceinline__ void walk_exact_fast(const uint32_t *__restrict__ ref, const uint32_t *__restrict__ qry,
-                                                uint32_t ar, uint32_t aq, uint32_t limit, uint32_t tlo,
-                                                uint32_t thi, const int *__restrict__ tab25, int X, int64_t &best,
-                                                uint64_t &best_n) {
-    int S = 0, M = 0;
-    uint32_t nb = 0, base = 0;
-    best = 0;
-    best_n = 0;
-    if (limit == 0) return;
-    const uint32_t jr = (RIGHT ? ar : ar - 8u) + (uint32_t)kPadBases;
-    const uint32_t jq = (RIGHT ? aq : aq - 8u) + (uint32_t)kPadBases;
-    const uint32_t shr = (jr & 7u) * 4u, shq = (jq & 7u) * 4u;
-    const uint32_t *pr = ref + (jr >> 3), *pq = qry + (jq >> 3);
-    uint32_t r0 = __ldg(pr), r1 = __ldg(pr + 1), q0 = __ldg(pq), q1 = __ldg(pq + 1);
-    uint32_t rem = limit;
-    for (;;) {
-        const uint32_t R = __funnelshift_r(r0, r1, shr);
-        const uint32_t Q = __funnelshift_r(q0, q1, shq);
-        uint32_t keep = 0xFFFFFFFFu;
-        if (rem < 8) keep = RIGHT ? ((1u << (4 * rem)) - 1u) : ~((1u << (4 * (8 - rem))) - 1u);
-        int Sv[8];
-        step_sums<RIGHT>(R, Q, keep, tlo, thi, tab25, S, Sv);
-        const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
-        const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
-        if (lo < max(M, hi) - X) {
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                if (M - Sv[k] > X) {
-                    best = M;
-                    best_n = nb;
-                    return;
-                }
-                if (Sv[k] > M) {
-                    M = Sv[k];
-                    nb = base + k + 1;
-                }
-            }
-        } else if (hi > M) {
-            int k = 7;
-#pragma unroll
-            for (int i = 6; i >= 0; i--)
-                if (Sv[i] == hi) k = i;
-            M = hi;
-            nb = base + k + 1;
-        }
-        if (rem <= 8) break;
-        rem -= 8;
-        base += 8;
-        S = Sv[7];
-        if (RIGHT) {
-            r0 = r1;
-            q0 = q1;
-            pr++;
-            pq++;
-            r1 = __ldg(pr + 1);
-            q1 = __ldg(pq + 1);
-        } else {
-            r1 = r0;
-            q1 = q0;
-            pr--;
-            pq--;
-            r0 = __ldg(pr);
-            q0 = __ldg(pq);
-        }
-    }
-    best = M;
-    best_n = nb;
-}
-
-// ------------------------------------------------------------------ warp materializer
-// One warp per survivor (E.1-E.5), in tiles of 256 bases: lane l holds the
-// 8 walk steps 8l+1..8l+8 of the tile.  The lanes' running sums come from
-// byte dot products plus a warp exclusive scan of the lane sums; the maximum
-// before each lane from an exclusive max-scan; each lane tests its own steps
-// for a drop against that maximum and a ballot picks the first dropping lane
-// (E.2: "ballot the first lane beyond X-drop").  The earliest step attaining
-// the side maximum is found by a second ballot (E.2 invariant).  Left walks
-// run forward over the reversed sequences.
-
-__device__ __forceinline__ int warp_excl_sum(int v, int lane, int *total) {
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, x, o);
-        if (lane >= o) x += y;
-    }
-    *total = __shfl_sync(kFullMask, x, 31);
-    return x - v;
-}
-
-__device__ __forceinline__ int warp_excl_max(int v, int lane, int init, int *all) {
-    int x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(kFullMask, x, o);
-        if (lane >= o) x = max(x, y);
-    }
-    *all = max(init, __shfl_sync(kFullMask, x, 31));
-    const int prev = __shfl_up_sync(kFullMask, x, 1);
-    return lane ? max(init, prev) : init;
-}
-
-// One side of survivor anchor (ar, aq); every lane returns the same result.
-// Inside a tile all values are relative to the running sum at the tile start
-// (int32: bounded by X plus one tile of scores); only the absolute running
-// sum and maximum are 64-bit, so walks of any length stay exact.
-__device__ __forceinline__ void warp_side(const Seqs &sq, const uint32_t *ref_rev, const uint32_t *qry_rev,
-                                          uint32_t ar, uint32_t aq, int side, uint32_t tlo, uint32_t thi,
-                                          const int *__restrict__ tab25, int X, int lane, int64_t &best,
-                                          uint32_t &best_n) {
-    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
-    const uint32_t rb = side ? ar : Lr - ar, qb = side ? aq : Lq - aq;
-    const uint32_t limit = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
-    const uint32_t jr = rb + (uint32_t)kPadBases, jq = qb + (uint32_t)kPadBases;
-    const uint32_t *wr = (side ? sq.ref : ref_rev) + (jr >> 3);
-    const uint32_t *wq = (side ? sq.qry : qry_rev) + (jq >> 3);
-    const uint32_t shr = (jr & 7u) * 4u, shq = (jq & 7u) * 4u;
-    int64_t St = 0, Mt = 0;
-    int Dt = 0;  // Mt - St, never above X while the walk goes on
-    uint32_t nb = 0;
-    for (uint32_t base0 = 0; base0 < limit; base0 += 256) {
-        const uint32_t off = base0 / 8 + (uint32_t)lane;
-        const uint32_t R = __funnelshift_r(__ldg(wr + off), __ldg(wr + off + 1), shr);
-        const uint32_t Q = __funnelshift_r(__ldg(wq + off), __ldg(wq + off + 1), shq);
-        const uint32_t first = base0 + 8u * (uint32_t)lane;  // steps before this lane's first
-        const uint32_t valid = limit > first ? min(limit - first, 8u) : 0u;
-        const uint32_t keep = valid >= 8 ? 0xFFFFFFFFu : ((1u << (4 * valid)) - 1u);
-        int L[8];
-        step_sums<true>(R, Q, keep, tlo, thi, tab25, 0, L);
-        int tot;
-        const int E = warp_excl_sum(L[7], lane, &tot);  // lane start, relative to the tile start
-        int lm = L[0];
-#pragma unroll
-        for (int k = 1; k < 8; k++) lm = max(lm, L[k]);
-        int pm_all;
-        const int PM = warp_excl_max(E + lm, lane, Dt, &pm_all);  // maximum before this lane (relative)
-        int kd = 8;  // first step of this lane that drops (8: none)
-        int ll = L[0];
-#pragma unroll
-        for (int k = 1; k < 8; k++) ll = min(ll, L[k]);
-        if (ll < max(PM - E, lm) - X) {  // a drop is possible in this lane: find it
-            int rk = PM - E;             // running maximum relative to this lane's start
-#pragma unroll
-            for (int k = 0; k < 8; k++) {
-                if (kd == 8 && rk - L[k] > X) kd = k;
-                rk = max(rk, L[k]);
-            }
-        }
-        const unsigned dm = __ballot_sync(kFullMask, kd < 8);
-        int Mnew;
-        int cut = 8;  // steps of this lane inside the walk
-        if (dm) {
-            const int f = __ffs(dm) - 1;
-            int mine = PM;
-#pragma unroll
-            for (int k = 0; k < 8; k++)
-                if (k < kd) mine = max(mine, E + L[k]);
-            Mnew = __shfl_sync(kFullMask, mine, f);
-            cut = lane < f ? 8 : (lane == f ? kd : 0);
-        } else {
-            Mnew = pm_all;
-        }
-        if (Mnew > Dt) {  // earliest step reaching the new maximum: its lane first, then the step
-            bool has = false;
-            if (cut == 8) has = E + lm == Mnew;
-            else if (cut > 0) {
-#pragma unroll
-                for (int k = 0; k < 8; k++)
-                    if (k < cut && E + L[k] == Mnew) has = true;
-            }
-            const unsigned fm = __ballot_sync(kFullMask, has);
-            const int fl = __ffs(fm) - 1;
-            int kf = 0;
-            if (lane == fl) {
-                kf = 7;
-#pragma unroll
-                for (int k = 6; k >= 0; k--)
-                    if (E + L[k] == Mnew) kf = k;
-            }
-            const int kk = __shfl_sync(kFullMask, kf, fl);
-            nb = base0 + 8u * (uint32_t)fl + (uint32_t)kk + 1u;
-            Mt = St + Mnew;
-        }
-        if (dm) break;
-        St += tot;
-        Dt = (int)(Mt - St);
-    }
-    best = Mt;
-    best_n = nb;
-}
-
-__global__ void __launch_bounds__(256) k_materialize_warp(const uint2 *__restrict__ anchors, uint64_t n_anchors,
-                                                          uint32_t id_base, const uint32_t *__restrict__ ids,
-                                                          uint64_t n_ids, Seqs sq,
-                                                          const uint32_t *__restrict__ ref_rev,
-                                                          const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
-                                                          uint4 *__restrict__ out, uint8_t *__restrict__ done) {
-    __shared__ int tab[25];
-    if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
-    __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const uint64_t warps = (uint64_t)gridDim.x * (blockDim.x / 32);
-    for (uint64_t k = (blockIdx.x * (uint64_t)blockDim.x + threadIdx.x) / 32; k < n_ids; k += warps) {
-        const uint32_t id = ids[k];
-        const uint64_t slot = (uint64_t)id - id_base;
-        const uint2 a = (id >= id_base && slot < n_anchors) ? anchors[slot] : make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-        uint4 rec = make_uint4(0, 0, 0, 0);
-        uint8_t ok = 0;
-        if (a.x < sq.Lr && a.y < sq.Lq) {
-            int64_t ML, MR;
-            uint32_t nL, nR;
-            warp_side(sq, ref_rev, qry_rev, a.x, a.y, 0, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, lane, ML, nL);
-            warp_side(sq, ref_rev, qry_rev, a.x, a.y, 1, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, lane, MR, nR);
-            int64_t score = ML + MR;
-            if (score > 2147483647LL) score = 2147483647LL;
-            if (score >= sa.T) {
-                rec = make_uint4(a.x - (uint32_t)nL, a.y - (uint32_t)nL, (uint32_t)(nL + nR - 1),
-                                 (uint32_t)(int32_t)score);
-                ok = 1;
-            }
-        }
-        if (lane == 0) {
-            out[k] = rec;
-            done[k] = ok;
-        }
-    }
-}
-
-// One thread per survivor (E.1-E.5).
-template <bool FAST>
+// One thread per survivor (E.1-E.5), any matrix: 64-bit base-by-base walks.
 __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ anchors, uint64_t n_anchors, uint32_t id_base,
                                                      const uint32_t *__restrict__ ids, uint64_t n_ids, Seqs sq,
                                                      ScoreArgs sa, uint4 *__restrict__ out,
@@ -803,15 +565,8 @@ __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ a
         if (a.x < sq.Lr && a.y < sq.Lq) {
             int64_t ML, MR;
             uint64_t nL, nR;
-            const uint32_t lim_l = min(a.x, a.y);
-            const uint32_t lim_r = (uint32_t)min(sq.Lr - a.x, sq.Lq - a.y);
-            if (FAST && lim_l < (1u << 24) && lim_r < (1u << 24)) {
-                walk_exact_fast<false>(sq.ref, sq.qry, a.x, a.y, lim_l, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, ML, nL);
-                walk_exact_fast<true>(sq.ref, sq.qry, a.x, a.y, lim_r, sa.tab_lo, sa.tab_hi, tab, sa.xdrop, MR, nR);
-            } else {
-                side_exact(sq, tab, sa.xdrop, a.x, a.y, false, ML, nL);
-                side_exact(sq, tab, sa.xdrop, a.x, a.y, true, MR, nR);
-            }
+            side_exact(sq, tab, sa.xdrop, a.x, a.y, false, ML, nL);
+            side_exact(sq, tab, sa.xdrop, a.x, a.y, true, MR, nR);
             int64_t score = ML + MR;
             if (score > 2147483647LL) score = 2147483647LL;
             if (score >= sa.T) {
@@ -846,7 +601,7 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
     const unsigned g = (unsigned)blocks;
     const uint32_t sb = c.seed_begin, se = c.seed_end, hb = c.hit_begin;
     if (!d_flags) {
-        k_expand_gate<false, false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
+        k_expand_gate<false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     } else if (sa.fast) {
         const uint64_t n_tiles = (n + kWTile - 1) / kWTile;
         k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
@@ -854,7 +609,7 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
                                                                     seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa,
                                                                     out, d_flags); count_launch();
     } else {
-        k_expand_gate<true, false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
+        k_expand_gate<true><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     }
     return cudaGetLastError();
 }
@@ -880,12 +635,11 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
     const uint2 *an = reinterpret_cast<const uint2 *>(d_anchors);
     uint4 *out = reinterpret_cast<uint4 *>(d_out);
     if (sa.fast) {
-        const uint64_t warps = n_ids < 152ull * 64 ? n_ids : 152ull * 64;
-        k_materialize_warp<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids,
-                                                                                  seqs(ref, qry), ref.rev, qry.rev, sa,
-                                                                                  out, d_done); count_launch();
+        const uint64_t blocks = (n_ids + 255) / 256;
+        k_materialize_lane<<<(unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64), 256, 0, st>>>(
+            an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry), ref.rev, qry.rev, sa, out, d_done); count_launch();
     } else {
-        k_materialize<false><<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry),
+        k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry),
                                                                     sa, out, d_done); count_launch();
     }
     return cudaGetLastError();
