@@ -547,6 +547,151 @@ __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict_
     best_n = nb;
 }
 
+// One lane per survivor (E.1-E.5).  The lane walks its left side, then its
+// right side, in one loop (both over forward-running copies), so lanes do not
+// wait for one another between the sides; consecutive survivors come from the
+// same homology and take similar total walks.  The earliest maximum is kept
+// lazily: the step in which the maximum last rose and the running sum at that
+// step's start; when the side ends that one step is scored again to find the
+// exact base (E.2 invariant).  A side that passes 2^20 steps (|S| could then
+// approach 2^31) sends the survivor to the 64-bit base-by-base walk.
+__global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restrict__ anchors, uint64_t n_anchors,
+                                                          uint32_t id_base, const uint32_t *__restrict__ ids,
+                                                          uint64_t n_ids, Seqs sq,
+                                                          const uint32_t *__restrict__ ref_rev,
+                                                          const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
+                                                          uint4 *__restrict__ out, uint8_t *__restrict__ done) {
+    __shared__ int tab[25];
+    if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
+    __syncthreads();
+    const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
+    const int X = sa.xdrop;
+    const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t k = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; k < n_ids; k += stride) {
+        const uint32_t id = ids[k];
+        const uint64_t slot = (uint64_t)id - id_base;
+        const uint2 a = (id >= id_base && slot < n_anchors) ? anchors[slot] : make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+        uint4 rec = make_uint4(0, 0, 0, 0);
+        uint8_t ok = 0;
+        if (a.x < sq.Lr && a.y < sq.Lq) {
+            int64_t ML = 0, MR = 0;
+            uint32_t nL = 0, nR = 0;
+            bool long_walk = false;
+            {
+                int side = 0;
+                WalkState w;
+                walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, 0);
+                w.r0 = __ldg(w.pr);
+                w.r1 = __ldg(w.pr + 1);
+                w.q0 = __ldg(w.pq);
+                w.q1 = __ldg(w.pq + 1);
+                int mstep = -1, mS = 0;
+                uint32_t steps = 0;
+                for (;;) {
+                    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
+                    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
+                    const uint32_t keep = w.rem >= 8 ? 0xFFFFFFFFu : ((1u << (4 * w.rem)) - 1u);
+                    int Sv[8];
+                    step_sums<true>(R, Q, keep, tlo, thi, tab, w.S, Sv);
+                    const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])),
+                                       max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
+                    const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])),
+                                       min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
+                    const int Mb = max(w.M, hi);
+                    const bool maybe_stop = lo < Mb - X;
+                    if (!(maybe_stop | (w.rem <= 8))) {
+                        if (hi > w.M) {
+                            mstep = (int)steps;
+                            mS = w.S;
+                        }
+                        w.M = Mb;
+                        walk_advance(w, Sv[7]);
+                        if (++steps >= (1u << 20)) {
+                            long_walk = true;
+                            break;
+                        }
+                        continue;
+                    }
+                    // a step that may hold the stop, or the edge: settle it base by base
+                    int Mf = w.M, kset = -1;
+                    bool dropped = false;
+#pragma unroll
+                    for (int j = 0; j < 8; j++) {
+                        if (Mf - Sv[j] > X) {
+                            dropped = true;
+                            break;
+                        }
+                        if (Sv[j] > Mf) {
+                            Mf = Sv[j];
+                            kset = j;
+                        }
+                    }
+                    if (!dropped && w.rem > 8) {  // no stop after all: walk on
+                        if (kset >= 0) {
+                            mstep = (int)steps;
+                            mS = w.S;
+                        }
+                        w.M = Mf;
+                        walk_advance(w, Sv[7]);
+                        if (++steps >= (1u << 20)) {
+                            long_walk = true;
+                            break;
+                        }
+                        continue;
+                    }
+                    uint32_t nbest = 0;
+                    if (kset >= 0) {
+                        nbest = steps * 8u + (uint32_t)kset + 1u;
+                    } else if (mstep >= 0) {  // score the step of the maximum again
+                        const uint32_t back = steps - (uint32_t)mstep;
+                        const uint32_t *pr = w.pr - back, *pq = w.pq - back;
+                        int Sm[8];
+                        step_sums<true>(__funnelshift_r(__ldg(pr), __ldg(pr + 1), w.shr),
+                                        __funnelshift_r(__ldg(pq), __ldg(pq + 1), w.shq), 0xFFFFFFFFu, tlo, thi,
+                                        tab, mS, Sm);
+                        int kk = 7;
+#pragma unroll
+                        for (int j = 6; j >= 0; j--)
+                            if (Sm[j] == Mf) kk = j;
+                        nbest = (uint32_t)mstep * 8u + (uint32_t)kk + 1u;
+                    }
+                    if (side == 1) {
+                        MR = Mf;
+                        nR = nbest;
+                        break;
+                    }
+                    ML = Mf;
+                    nL = nbest;
+                    side = 1;
+                    walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, 1);
+                    w.r0 = __ldg(w.pr);
+                    w.r1 = __ldg(w.pr + 1);
+                    w.q0 = __ldg(w.pq);
+                    w.q1 = __ldg(w.pq + 1);
+                    mstep = -1;
+                    mS = 0;
+                    steps = 0;
+                }
+            }
+            if (long_walk) {
+                uint64_t n0, n1;
+                side_exact(sq, tab, sa.xdrop, a.x, a.y, false, ML, n0);
+                side_exact(sq, tab, sa.xdrop, a.x, a.y, true, MR, n1);
+                nL = (uint32_t)n0;
+                nR = (uint32_t)n1;
+            }
+            int64_t score = ML + MR;
+            if (score > 2147483647LL) score = 2147483647LL;
+            if (score >= sa.T) {
+                rec = make_uint4(a.x - nL, a.y - nL, nL + nR - 1u, (uint32_t)(int32_t)score);
+                ok = 1;
+            }
+        }
+        out[k] = rec;
+        done[k] = ok;
+    }
+}
+
 // One thread per survivor (E.1-E.5), any matrix: 64-bit base-by-base walks.
 __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ anchors, uint64_t n_anchors, uint32_t id_base,
                                                      const uint32_t *__restrict__ ids, uint64_t n_ids, Seqs sq,
