@@ -183,6 +183,8 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gate", default="fused", choices=["fused", "bucketed"],
+                    help="fused expansion + gate (default), or expansion then the reference-bucketed gate (D.5)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -228,7 +230,11 @@ def main():
                 if timed_gate:
                     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                     e0.record(stream)
-                hspz.hspz_expand_gate(plan, c, eng.params, anchors, flags)
+                if args.gate == "fused":
+                    hspz.hspz_expand_gate(plan, c, eng.params, anchors, flags)
+                else:
+                    hspz.hspz_expand(plan, c, anchors)
+                    hspz.hspz_score_gate_bucketed(eng.index, plan, anchors, n, eng.params, flags)
                 if timed_gate:
                     e1.record(stream)
                     ev_gate.append((e0, e1, n))
@@ -335,7 +341,8 @@ def main():
         "expand_gate_anchors_per_s": n_anchors * args.steps / (sum(gate_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": "k_expand_gate (fused expansion + score gate)",
+                     "kernel": ("k_expand_gate_w (fused expansion + score gate)" if args.gate == "fused" else
+                                "expansion + bucket sort + k_gate_rounds (reference-bucketed gate)"),
                      "kernel_ms_per_launch": sum(gate_ms) / n_launch,
                      "algorithmic_bytes_per_launch": alg_bytes_per_launch},
         "cpu_baseline": cpu,

@@ -188,6 +188,18 @@ int hspz_score_gate(const hspz_index *index, const hspz_plan *plan, const hspz_a
                     const hspz_score_params *params, uint8_t *d_flags, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Reference-bucketed score gate ("D. Score gate", D.5): the same flags as
+ * hspz_score_gate, computed after a stable counting sort of the anchors into
+ * n_buckets reference-address windows (1..32; 0 = auto: enough windows that
+ * one window of the packed reference, both directions, fits 3/4 of the L2).
+ * The gate writes each flag at the anchor's raw position.  Needs a matrix the
+ * fast gate takes (complement symmetric on A/C/G/T with int8 scores), else
+ * HSPZ_E_UNSUPPORTED.  Uses stream-ordered scratch of 12 bytes per anchor.
+ * ------------------------------------------------------------------------ */
+int hspz_score_gate_bucketed(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors, uint64_t n,
+                             const hspz_score_params *params, uint32_t n_buckets, uint8_t *d_flags, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Stable compaction ("D. Score gate", D.4): d_ids receives id_base + i for
  * every i < n with d_flags[i] != 0, in increasing order; *n_out receives the
  * count.  If the count exceeds cap nothing is written and HSPZ_E_CAPACITY is

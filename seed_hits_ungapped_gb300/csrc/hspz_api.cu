@@ -397,8 +397,43 @@ int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor 
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
     SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
-    cudaError_t e = launch_gate(d_anchors, n, r, q, sa, d_flags, (cudaStream_t)stream);
+    cudaError_t e = launch_gate(d_anchors, nullptr, n, r, q, sa, d_flags, (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate");
+}
+
+int hspz_score_gate_bucketed(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n,
+                             const hspz_score_params *params, uint32_t n_buckets, uint8_t *d_flags, void *stream) {
+    if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags)) || n_buckets > 32 || n > (1ull << 32))
+        return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    if (!sa.fast) {
+        set_error("hspz_score_gate_bucketed: the matrix is not complement symmetric with int8 scores");
+        return HSPZ_E_UNSUPPORTED;
+    }
+    if (!n) return HSPZ_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (n_buckets == 0) {  // auto: windows of the packed reference (both directions) in 3/4 of the L2
+        int dev = 0, l2 = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+        const double window = 0.75 * (l2 > 0 ? l2 : (64 << 20));
+        const double bytes = 2.0 * (double)ix->ref_words * 4.0;
+        n_buckets = (uint32_t)std::min(32.0, std::max(1.0, std::ceil(bytes / window)));
+    }
+    const uint64_t Lr = std::max<uint64_t>(ix->ref_len, 1);
+    const uint32_t span = (uint32_t)((Lr + n_buckets - 1) / n_buckets);
+    hspz_anchor *sorted = nullptr;
+    uint32_t *raw = nullptr, *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync((void **)&sorted, n * sizeof(hspz_anchor), st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&raw, n * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&scratch, bucket_scratch_words(n, n_buckets) * 4, st);
+    if (e == cudaSuccess) e = launch_bucket_sort(d_anchors, n, span, n_buckets, sorted, raw, scratch, st);
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    if (e == cudaSuccess) e = launch_gate(sorted, raw, n, r, q, sa, d_flags, st);
+    for (void *ptr : {(void *)sorted, (void *)raw, (void *)scratch})
+        if (ptr) cudaFreeAsync(ptr, st);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate_bucketed");
 }
 
 int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,

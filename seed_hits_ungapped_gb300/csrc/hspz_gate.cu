@@ -516,6 +516,68 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
     for (uint32_t i = lane; i < count; i += 32) out[t0 + i] = sA[i];
 }
 
+// Round-based fast gate over an anchor array in global memory (the standalone
+// gate, and the gate of the reference-bucketed mode, whose anchors arrive
+// sorted by reference window with their raw ids).  One warp per unit of 256
+// anchors, 8 synchronous rounds of 32 as in k_expand_gate_w; the flag of
+// anchor i goes to flags[raw ? raw[i] : i].
+__global__ void __launch_bounds__(kWWarps * 32, 5)
+    k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq,
+                  const uint32_t *__restrict__ ref_rev, const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
+                  uint8_t *__restrict__ flags) {
+    __shared__ int tab[25];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < 25) tab[tid] = sa.m[tid];
+    __syncthreads();
+    const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
+    const int X = sa.xdrop, T = sa.T;
+    const uint64_t n_units = (n + kWUnit - 1) / kWUnit;
+    for (uint64_t u = (uint64_t)blockIdx.x * kWWarps + warp; u < n_units; u += (uint64_t)gridDim.x * kWWarps) {
+        const uint64_t t0 = u * kWUnit;
+        const uint32_t count = (uint32_t)min((uint64_t)kWUnit, n - t0);
+        for (uint32_t round = 0; round * 32 < count; round++) {
+            const uint32_t ai = round * 32u + (uint32_t)lane;
+            const bool valid = ai < count;
+            uint2 a = make_uint2(0, 0);
+            if (valid) a = anchors[t0 + ai];
+            const bool inside = valid && a.x < sq.Lr && a.y < sq.Lq;
+            bool accepted = false;
+            int need = T;
+#pragma unroll 1
+            for (int side = 0; side < 2; side++) {
+                const bool walk = inside && !accepted;
+                WalkState w;
+                if (walk) {
+                    walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
+                    w.r0 = __ldg(w.pr);
+                    w.r1 = __ldg(w.pr + 1);
+                    w.q0 = __ldg(w.pq);
+                    w.q1 = __ldg(w.pq + 1);
+                }
+                bool ended = !walk, stepping = walk;
+                int Sv[8], Mb = 0;
+                bool maybe_stop = false;
+                while (__any_sync(kFullMask, !ended)) {
+                    while (__any_sync(kFullMask, stepping)) {
+                        if (stepping && walk_step(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+                    }
+                    if (!ended) {
+                        bool acc = false;
+                        if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
+                            ended = true;
+                            accepted = acc;
+                            if (side == 0) need = T - w.M;
+                        } else {
+                            stepping = true;
+                        }
+                    }
+                }
+            }
+            if (valid) flags[raw ? raw[t0 + ai] : t0 + ai] = accepted ? 1 : 0;
+        }
+    }
+}
+
 template <bool FAST>
 __global__ void __launch_bounds__(256) k_gate(const uint2 *__restrict__ anchors, uint64_t n, Seqs sq, ScoreArgs sa,
                                               uint8_t *__restrict__ flags) {
@@ -759,15 +821,19 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
     return cudaGetLastError();
 }
 
-cudaError_t launch_gate(const hspz_anchor *d_anchors, uint64_t n, SeqView ref, SeqView qry, const ScoreArgs &sa,
-                        uint8_t *d_flags, cudaStream_t st) {
+cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uint64_t n, SeqView ref, SeqView qry,
+                        const ScoreArgs &sa, uint8_t *d_flags, cudaStream_t st) {
     if (!n) return cudaSuccess;
     if (sa.fast) {
-        k_gate<true><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
-                                                        d_flags); count_launch();
-    } else {
+        const uint64_t units = (n + kWUnit - 1) / kWUnit, want = (units + kWWarps - 1) / kWWarps;
+        const unsigned g = (unsigned)(want < 152ull * 40 ? want : 152ull * 40);
+        k_gate_rounds<<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n, seqs(ref, qry),
+                                                   ref.rev, qry.rev, sa, d_flags); count_launch();
+    } else if (!d_raw) {
         k_gate<false><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
                                                          d_flags); count_launch();
+    } else {
+        return cudaErrorInvalidValue;  // raw ids come only with the fast gate
     }
     return cudaGetLastError();
 }

@@ -307,6 +307,11 @@ cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, 
     return cudaGetLastError();
 }
 
+cudaError_t launch_scan_u32(const uint32_t *d_in, uint64_t n, uint32_t *d_excl, cudaStream_t st) {
+    k_scan<uint32_t, uint32_t><<<1, 1024, 0, st>>>(d_in, n, d_excl, nullptr, nullptr); count_launch();
+    return cudaGetLastError();
+}
+
 cudaError_t launch_prefix(const uint32_t *d_cnt, uint64_t n_seeds, const uint64_t *d_block_excl, uint32_t *d_P,
                           cudaStream_t st) {
     uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;

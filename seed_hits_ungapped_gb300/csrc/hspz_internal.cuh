@@ -78,8 +78,15 @@ uint64_t expand_gate_tile_words(uint64_t max_chunk_hits);
 cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const uint32_t *d_pos,
                                const hspz_chunk &c, int span, SeqView ref, SeqView qry, const ScoreArgs &sa,
                                hspz_anchor *d_out, uint8_t *d_flags, uint32_t *d_tiles, cudaStream_t st);
-cudaError_t launch_gate(const hspz_anchor *d_anchors, uint64_t n, SeqView ref, SeqView qry, const ScoreArgs &sa,
-                        uint8_t *d_flags, cudaStream_t st);
+// d_raw (nullable, fast matrices only): flag of anchor i goes to d_flags[d_raw[i]]
+cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uint64_t n, SeqView ref, SeqView qry,
+                        const ScoreArgs &sa, uint8_t *d_flags, cudaStream_t st);
+// reference-locality buckets (D.5): stable counting sort of n anchors by ref_end / span into n_buckets
+// buckets; d_sorted/d_raw receive the anchors and their raw ids; d_scratch holds bucket_scratch_words(n)
+uint64_t bucket_scratch_words(uint64_t n, uint32_t n_buckets);
+cudaError_t launch_bucket_sort(const hspz_anchor *d_anchors, uint64_t n, uint32_t span, uint32_t n_buckets,
+                               hspz_anchor *d_sorted, uint32_t *d_raw, uint32_t *d_scratch, cudaStream_t st);
+cudaError_t launch_scan_u32(const uint32_t *d_in, uint64_t n, uint32_t *d_excl, cudaStream_t st);
 cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
                                uint64_t n_ids, SeqView ref, SeqView qry, const ScoreArgs &sa,
                                hspz_segment_pair *d_out, uint8_t *d_done, cudaStream_t st);

@@ -34,7 +34,7 @@ EXPORTS = [
     "hspz_index_free", "hspz_index_info", "hspz_index_tables", "hspz_find_hits", "hspz_plan_free",
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
-    "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags",
+    "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed",
 ]
 
 
@@ -92,6 +92,7 @@ def load_library():
         "hspz_kernel_launches": (U64, []),
         "hspz_compact_noalloc": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_compact_noalloc_max_flags": (U64, []),
+        "hspz_score_gate_bucketed": (ctypes.c_int, [VP, VP, VP, U64, P(hspz_score_params), U32, VP, VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -286,6 +287,19 @@ def hspz_score_gate(index: Index, plan: Plan, d_anchors, n: int, params: hspz_sc
     rc = load_library().hspz_score_gate(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"), int(n),
                                         ctypes.byref(params), _dptr(d_flags, torch.uint8, "d_flags"), _stream(stream))
     _check(rc, "hspz_score_gate")
+
+
+def hspz_score_gate_bucketed(index: Index, plan: Plan, d_anchors, n: int, params: hspz_score_params, d_flags,
+                             n_buckets: int = 0, stream=None):
+    """D.5: the flags of hspz_score_gate, gated bucket by bucket of reference window."""
+    import torch
+    if d_anchors.numel() < 2 * n or d_flags.numel() < n:
+        raise ValueError("buffers shorter than n")
+    rc = load_library().hspz_score_gate_bucketed(index.handle, plan.handle,
+                                                 _dptr(d_anchors, torch.int32, "d_anchors"), int(n),
+                                                 ctypes.byref(params), int(n_buckets),
+                                                 _dptr(d_flags, torch.uint8, "d_flags"), _stream(stream))
+    _check(rc, "hspz_score_gate_bucketed")
 
 
 def hspz_compact(d_flags, n: int, id_base: int, d_ids, stream=None) -> int:

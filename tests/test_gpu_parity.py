@@ -244,3 +244,26 @@ def test_workload_a_full_size_sampled(torch_cuda):
     pick = np.unique(rng.integers(0, ch.ids.size, 5_000))
     rec, done = oracle.materialize(w.ref, w.query, ch.anchors, 0, ch.ids[pick], w.matrix, w.xdrop, eng.T)
     assert np.array_equal(ch.records[pick], rec) and np.array_equal(ch.done[pick], done)
+
+
+@pytest.mark.parametrize("name,scale", [("workload_a", 0.02), ("mid", 0.1), ("dense", 0.03)])
+def test_reference_bucketed_gate_equals_fused(torch_cuda, name, scale):
+    """D.5: bucketing by reference window leaves every flag unchanged."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    w = synth.make(name, scale=scale)
+    eng = _engine(torch, w.ref, w.matrix, w.xdrop, w.K)
+    plan = eng.plan(_dev(torch, w.query))
+    n = plan.total_hits
+    anchors = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+    fused = torch.empty(n, dtype=torch.uint8, device="cuda")
+    hspz.hspz_expand_gate(plan, 0, eng.params, anchors, fused)
+    want = oracle.gate(w.ref, w.query, anchors.cpu().numpy().view(np.uint32), w.matrix, w.xdrop, eng.T)
+    assert np.array_equal(fused.cpu().numpy(), want)
+    for nb in (0, 1, 3, 32):
+        got = torch.full((n,), 9, dtype=torch.uint8, device="cuda")
+        hspz.hspz_score_gate_bucketed(eng.index, plan, anchors, n, eng.params, got, n_buckets=nb)
+        assert torch.equal(got, fused), nb
+    bad = hspz.score_params(np.arange(25).reshape(5, 5) - 12, w.xdrop, w.K)  # not complement symmetric
+    with pytest.raises(hspz.HspzError):
+        hspz.hspz_score_gate_bucketed(eng.index, plan, anchors, n, bad, fused)
