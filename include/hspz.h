@@ -142,7 +142,10 @@ int hspz_index_tables(const hspz_index *index, const uint32_t **d_idx, const uin
  * *total_hits still reports the total), and cuts MAX_HITS chunks: one chunk if
  * total <= max_hits or max_hits == 0, else the lower-bound walk over the seed
  * prefixes that keeps the straddling seed whole.  flags: 0 or HSPZ_WALK_FULL.
- * The plan keeps pointers into `index`.  Synchronizes `stream`.
+ * The plan keeps pointers into `index`.  Its device buffers come from the
+ * device's stream-ordered memory pool on `stream`, and hspz_plan_free returns
+ * them in that stream's order, so free a plan only with its work queued on
+ * that stream (or finished).  Synchronizes `stream`.
  * ------------------------------------------------------------------------ */
 int hspz_find_hits(const hspz_index *index, const uint8_t *d_query, uint64_t query_len, uint64_t max_hits,
                    uint32_t flags, hspz_plan **plan_out, uint64_t *total_hits, void *stream);

@@ -238,9 +238,11 @@ int hspz_index_tables(const hspz_index *ix, const uint32_t **d_idx, const uint32
 
 void hspz_plan_free(hspz_plan *p) {
     if (!p) return;
+    // stream-ordered: the buffers go back to the device pool once the work
+    // queued on the plan's stream so far has finished
     for (void *q : {(void *)p->d_P, (void *)p->d_lo, (void *)p->d_cnt, (void *)p->d_blk, (void *)p->d_qry,
                     (void *)p->d_qry_rev, (void *)p->d_tiles})
-        if (q) cudaFree(q);
+        if (q) cudaFreeAsync(q, p->stream);
     delete p;
 }
 
@@ -261,12 +263,13 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     p->qry_words = packed_words(query_len);
     cudaError_t e = cudaSuccess;
     const uint64_t sa = S ? S : 1;
-    e = cudaMalloc((void **)&p->d_P, sa * 4);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_lo, sa * 4);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_cnt, sa * 4);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_blk, (3 * nb + 1) * 8);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_qry, p->qry_words * 4);
-    if (e == cudaSuccess) e = cudaMalloc((void **)&p->d_qry_rev, p->qry_words * 4);
+    p->stream = st;
+    e = cudaMallocAsync((void **)&p->d_P, sa * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_lo, sa * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_cnt, sa * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_blk, (3 * nb + 1) * 8, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry, p->qry_words * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry_rev, p->qry_words * 4, st);
     if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 0, p->d_qry, p->qry_words, st);
     if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 1, p->d_qry_rev, p->qry_words, st);
     uint64_t *bsum = p->d_blk, *bexcl = p->d_blk + nb, *bincl = p->d_blk + 2 * nb, *dtot = p->d_blk + 3 * nb;
@@ -325,7 +328,7 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     p->max_chunk_hits = 0;
     for (const auto &c : p->chunks)
         p->max_chunk_hits = std::max<uint64_t>(p->max_chunk_hits, (uint64_t)c.hit_end - c.hit_begin);
-    e = cudaMalloc((void **)&p->d_tiles, expand_gate_tile_words(p->max_chunk_hits) * 4);
+    e = cudaMallocAsync((void **)&p->d_tiles, expand_gate_tile_words(p->max_chunk_hits) * 4, st);
     if (e != cudaSuccess) {
         rc = cuda_fail(e, "hspz_find_hits tile scratch");
         hspz_plan_free(p);

@@ -125,4 +125,5 @@ struct hspz_plan {
     std::vector<hspz_chunk> chunks;
     uint64_t max_chunk_hits;
     uint32_t *d_tiles;      // fused-kernel scratch: first/last seed of every tile of a chunk
+    cudaStream_t stream;    // the stream the plan was made on; its buffers are freed in its order
 };
