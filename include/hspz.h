@@ -178,6 +178,26 @@ int hspz_expand_gate(const hspz_plan *plan, uint32_t chunk, const hspz_score_par
                      hspz_anchor *d_anchors, uint8_t *d_flags, uint64_t cap, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * One chunk through the rest of the path with a single host synchronization:
+ * the fused expansion + gate (hspz_expand_gate), the stable compaction of the
+ * flags into survivor ids (hspz_compact), their materialization
+ * (hspz_materialize) and the stable compaction of the done flags into
+ * accepted indices (positions in the survivor list).  The survivor count
+ * stays on the device between the steps.  d_anchors and d_flags need room
+ * for the chunk's hits (cap_anchors); d_ids, d_records (16-byte aligned),
+ * d_done and d_accepted for cap_survivors entries.  *n_survivors and
+ * *n_accepted receive the counts.  If the survivors exceed cap_survivors,
+ * HSPZ_E_CAPACITY is returned with *n_survivors set: the anchors and flags are
+ * written, the survivor outputs are not; call again with more room.  gate_ms
+ * (may be NULL) receives the fused kernel's own event-timed duration.  Uses
+ * stream-ordered scratch; synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_process_chunk(const hspz_plan *plan, uint32_t chunk, const hspz_score_params *params,
+                       hspz_anchor *d_anchors, uint8_t *d_flags, uint64_t cap_anchors, uint32_t *d_ids,
+                       hspz_segment_pair *d_records, uint8_t *d_done, uint32_t *d_accepted, uint64_t cap_survivors,
+                       uint64_t *n_survivors, uint64_t *n_accepted, float *gate_ms, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Score-only X-drop gate ("D. Score gate", D.2-D.3) over n anchors against the
  * index's reference and the plan's query.  Per anchor (a_r, a_q): the right
  * side scores the anchor base and the bases after it, the left side the bases

@@ -394,6 +394,63 @@ int hspz_expand_gate(const hspz_plan *p, uint32_t chunk, const hspz_score_params
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_expand_gate");
 }
 
+int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_params *params, hspz_anchor *d_anchors,
+                       uint8_t *d_flags, uint64_t cap_anchors, uint32_t *d_ids, hspz_segment_pair *d_records,
+                       uint8_t *d_done, uint32_t *d_accepted, uint64_t cap_survivors, uint64_t *n_survivors,
+                       uint64_t *n_accepted, float *gate_ms, void *stream) {
+    if (!p || chunk >= p->chunks.size() || !n_survivors || !n_accepted) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    const hspz_chunk &c = p->chunks[chunk];
+    const uint64_t hits = (uint64_t)c.hit_end - c.hit_begin;
+    if (cap_anchors < hits) return HSPZ_E_CAPACITY;
+    if (hits && (!d_anchors || !d_flags)) return HSPZ_E_INVAL;
+    if (cap_survivors && (!d_ids || !d_records || !d_done || !d_accepted)) return HSPZ_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(d_records) & 15u) return HSPZ_E_INVAL;
+    *n_survivors = *n_accepted = 0;
+    if (gate_ms) *gate_ms = 0.f;
+    if (!hits) return HSPZ_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    const uint64_t words = compact_scratch_words(std::max(hits, cap_survivors)) + 8;
+    uint32_t *scratch = nullptr;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr;
+    uint64_t totals[2] = {0, 0};
+    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    // the two counts sit after the compaction scratch, 8-byte aligned
+    uint64_t *tot = reinterpret_cast<uint64_t *>(scratch + ((words - 6) & ~1ull));
+    if (e == cudaSuccess && gate_ms) {
+        e = cudaEventCreate(&ev0);
+        if (e == cudaSuccess) e = cudaEventCreate(&ev1);
+        if (e == cudaSuccess) e = cudaEventRecord(ev0, st);
+    }
+    if (e == cudaSuccess)
+        e = launch_expand_gate(p->d_P, p->d_lo, p->index->d_pos, c, p->index->shape.span, r, q, sa, d_anchors,
+                               d_flags, p->d_tiles, st);
+    if (e == cudaSuccess && gate_ms) e = cudaEventRecord(ev1, st);
+    if (e == cudaSuccess) e = launch_compact(d_flags, hits, c.hit_begin, d_ids, cap_survivors, scratch, tot, st);
+    if (e == cudaSuccess && cap_survivors) {
+        e = launch_materialize(d_anchors, hits, c.hit_begin, d_ids, cap_survivors, r, q, sa, d_records, d_done, st,
+                               tot);
+        if (e == cudaSuccess)
+            e = launch_compact(d_done, cap_survivors, 0, d_accepted, cap_survivors, scratch, tot + 1, st, tot);
+    } else if (e == cudaSuccess) {
+        e = cudaMemsetAsync(tot + 1, 0, 8, st);
+    }
+    if (e == cudaSuccess) e = cudaMemcpyAsync(totals, tot, 16, cudaMemcpyDeviceToHost, st);
+    cudaError_t ef = scratch ? cudaFreeAsync(scratch, st) : cudaSuccess;
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess && gate_ms) e = cudaEventElapsedTime(gate_ms, ev0, ev1);
+    if (ev0) cudaEventDestroy(ev0);
+    if (ev1) cudaEventDestroy(ev1);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_process_chunk");
+    *n_survivors = totals[0];
+    if (totals[0] > cap_survivors) return HSPZ_E_CAPACITY;
+    *n_accepted = totals[1];
+    return HSPZ_OK;
+}
+
 int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n,
                     const hspz_score_params *params, uint8_t *d_flags, void *stream) {
     if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags))) return HSPZ_E_INVAL;

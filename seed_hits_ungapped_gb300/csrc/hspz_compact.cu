@@ -11,6 +11,14 @@ constexpr int kPerThread = 16;
 constexpr int kTile = kThreads * kPerThread;  // 4096 flags per block
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
+// The count of flags: n, or (when d_n is given) the count at d_n if it is at
+// most n, else 0 (a count that overran its buffer yields nothing).
+__device__ __forceinline__ uint64_t count_of(uint64_t n, const uint64_t *d_n) {
+    if (!d_n) return n;
+    const uint64_t v = *d_n;
+    return v <= n ? v : 0;
+}
+
 // The 16 flags a thread owns, as a 16-bit mask (bit i = flag i != 0).
 template <bool ALIGNED>
 __device__ __forceinline__ uint32_t load_mask(const uint8_t *__restrict__ f, uint64_t i0, uint64_t n) {
@@ -34,8 +42,10 @@ __device__ __forceinline__ uint32_t load_mask(const uint8_t *__restrict__ f, uin
 
 template <bool ALIGNED>
 __global__ void __launch_bounds__(kThreads) k_count_flags(const uint8_t *__restrict__ f, uint64_t n,
+                                                          const uint64_t *__restrict__ d_n,
                                                           uint32_t *__restrict__ counts) {
     __shared__ uint32_t ws[kThreads / 32];
+    n = count_of(n, d_n);
     const uint64_t i0 = blockIdx.x * (uint64_t)kTile + (uint64_t)threadIdx.x * kPerThread;
     uint32_t c = __popc(load_mask<ALIGNED>(f, i0, n));
 #pragma unroll
@@ -85,11 +95,13 @@ __global__ void __launch_bounds__(1024) k_scan_counts(const uint32_t *__restrict
 }
 
 template <bool ALIGNED>
-__global__ void __launch_bounds__(kThreads) k_emit(const uint8_t *__restrict__ f, uint64_t n, uint32_t id_base,
+__global__ void __launch_bounds__(kThreads) k_emit(const uint8_t *__restrict__ f, uint64_t n,
+                                                   const uint64_t *__restrict__ d_n, uint32_t id_base,
                                                    const uint64_t *__restrict__ excl,
                                                    const uint64_t *__restrict__ total, uint64_t cap,
                                                    uint32_t *__restrict__ ids) {
     if (*total > cap) return;  // nothing is written when the output does not fit
+    n = count_of(n, d_n);
     __shared__ uint32_t ws[kThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t i0 = blockIdx.x * (uint64_t)kTile + (uint64_t)threadIdx.x * kPerThread;
@@ -121,7 +133,7 @@ uint64_t compact_scratch_words(uint64_t n) {
 }
 
 cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
-                           uint32_t *d_scratch, uint64_t *d_total, cudaStream_t st) {
+                           uint32_t *d_scratch, uint64_t *d_total, cudaStream_t st, const uint64_t *d_n) {
     if (!n) return cudaMemsetAsync(d_total, 0, 8, st);
     const uint64_t nb = (n + kTile - 1) / kTile;
     uint32_t *counts = d_scratch;
@@ -129,9 +141,9 @@ cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base,
     uint64_t *excl = reinterpret_cast<uint64_t *>(d_scratch + ((nb + 1) & ~1ull));
     const bool aligned = (reinterpret_cast<uintptr_t>(d_flags) & 15u) == 0;
     if (aligned) {
-        k_count_flags<true><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, counts); count_launch();
+        k_count_flags<true><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, d_n, counts); count_launch();
     } else {
-        k_count_flags<false><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, counts); count_launch();
+        k_count_flags<false><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, d_n, counts); count_launch();
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -139,9 +151,9 @@ cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base,
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (aligned) {
-        k_emit<true><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, id_base, excl, d_total, cap, d_ids); count_launch();
+        k_emit<true><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, d_n, id_base, excl, d_total, cap, d_ids); count_launch();
     } else {
-        k_emit<false><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, id_base, excl, d_total, cap, d_ids); count_launch();
+        k_emit<false><<<(unsigned)nb, kThreads, 0, st>>>(d_flags, n, d_n, id_base, excl, d_total, cap, d_ids); count_launch();
     }
     return cudaGetLastError();
 }

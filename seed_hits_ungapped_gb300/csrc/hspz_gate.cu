@@ -619,7 +619,7 @@ __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict_
 // approach 2^31) sends the survivor to the 64-bit base-by-base walk.
 __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                           uint32_t id_base, const uint32_t *__restrict__ ids,
-                                                          uint64_t n_ids, Seqs sq,
+                                                          uint64_t n_ids, const uint64_t *__restrict__ d_n, Seqs sq,
                                                           const uint32_t *__restrict__ ref_rev,
                                                           const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
                                                           uint4 *__restrict__ out, uint8_t *__restrict__ done) {
@@ -629,6 +629,7 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
     const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
     const int X = sa.xdrop;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+    if (d_n) n_ids = *d_n <= n_ids ? *d_n : 0;
     for (uint64_t k = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; k < n_ids; k += stride) {
         const uint32_t id = ids[k];
         const uint64_t slot = (uint64_t)id - id_base;
@@ -756,12 +757,13 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
 
 // One thread per survivor (E.1-E.5), any matrix: 64-bit base-by-base walks.
 __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ anchors, uint64_t n_anchors, uint32_t id_base,
-                                                     const uint32_t *__restrict__ ids, uint64_t n_ids, Seqs sq,
-                                                     ScoreArgs sa, uint4 *__restrict__ out,
-                                                     uint8_t *__restrict__ done) {
+                                                     const uint32_t *__restrict__ ids, uint64_t n_ids,
+                                                     const uint64_t *__restrict__ d_n, Seqs sq, ScoreArgs sa,
+                                                     uint4 *__restrict__ out, uint8_t *__restrict__ done) {
     __shared__ int tab[25];
     if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
     __syncthreads();
+    if (d_n) n_ids = *d_n <= n_ids ? *d_n : 0;
     for (uint64_t k = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; k < n_ids;
          k += (uint64_t)gridDim.x * blockDim.x) {
         const uint32_t id = ids[k];
@@ -841,16 +843,16 @@ cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uin
 cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
                                uint64_t n_ids,
                                SeqView ref, SeqView qry, const ScoreArgs &sa, hspz_segment_pair *d_out,
-                               uint8_t *d_done, cudaStream_t st) {
+                               uint8_t *d_done, cudaStream_t st, const uint64_t *d_n) {
     if (!n_ids) return cudaSuccess;
     const uint2 *an = reinterpret_cast<const uint2 *>(d_anchors);
     uint4 *out = reinterpret_cast<uint4 *>(d_out);
     if (sa.fast) {
         const uint64_t blocks = (n_ids + 255) / 256;
         k_materialize_lane<<<(unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64), 256, 0, st>>>(
-            an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry), ref.rev, qry.rev, sa, out, d_done); count_launch();
+            an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa, out, d_done); count_launch();
     } else {
-        k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, seqs(ref, qry),
+        k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry),
                                                                     sa, out, d_done); count_launch();
     }
     return cudaGetLastError();

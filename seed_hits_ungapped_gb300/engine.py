@@ -95,22 +95,35 @@ class HspEngine:
     def plan(self, d_query, max_hits: int = 0, walk_full: bool = False):
         return hspz.hspz_find_hits(self.index, d_query, max_hits, walk_full, stream=self.stream)
 
-    def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False) -> BatchResult:
+    def process_chunk(self, plan, c: int, time_gate: bool = False):
+        """hspz_process_chunk on the engine's buffers, growing the survivor
+        buffers and running the chunk again when they are too small.
+        Returns (n_anchors, n_survivors, n_accepted, gate_ms)."""
         torch = self.torch
+        n = int(plan.chunks[c, 3]) - int(plan.chunks[c, 2])
+        anchors = self.buffer("anchors", n, torch.int32, 2)
+        flags = self.buffer("flags", n, torch.uint8)
+        cap = self._bufs["ids"].shape[0] if "ids" in self._bufs else max(1024, n // 32)
+        while True:
+            bufs = [self.buffer("ids", cap, torch.int32), self.buffer("records", cap, torch.int32, 4),
+                    self.buffer("done", cap, torch.uint8), self.buffer("accepted", cap, torch.int32)]
+            try:
+                ns, na, ms = hspz.hspz_process_chunk(plan, c, self.params, anchors, flags, *bufs,
+                                                     stream=self.stream, time_gate=time_gate)
+                return n, ns, na, ms
+            except hspz.HspzError as e:
+                if e.status != hspz.HSPZ_E_CAPACITY:
+                    raise
+                cap = int(e.needed * 1.1) + 1024
+
+    def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False) -> BatchResult:
         plan = self.plan(d_query, max_hits, walk_full)
         out = []
         for c in range(plan.n_chunks):
-            hb, he = int(plan.chunks[c, 2]), int(plan.chunks[c, 3])
-            n = he - hb
-            anchors = self.buffer("anchors", n, torch.int32, 2)
-            flags = self.buffer("flags", n, torch.uint8)
-            hspz.hspz_expand_gate(plan, c, self.params, anchors, flags, stream=self.stream)
-            ids, n_surv = self._compact(flags, n, hb, "ids")
-            rec = self.buffer("records", n_surv, torch.int32, 4)
-            done = self.buffer("done", n_surv, torch.uint8)
-            hspz.hspz_materialize(self.index, plan, anchors, hb, ids, n_surv, self.params, rec, done,
-                                  stream=self.stream)
-            acc, n_acc = self._compact(done, n_surv, 0, "accepted")
+            hb = int(plan.chunks[c, 2])
+            n, n_surv, n_acc, _ = self.process_chunk(plan, c)
+            anchors, flags = self._bufs["anchors"], self._bufs["flags"]
+            ids, rec, done, acc = (self._bufs[k] for k in ("ids", "records", "done", "accepted"))
             r = ChunkResult(hb, n, n_surv, n_acc)
             if keep:
                 r.anchors = _np_u32(anchors[:n]).reshape(-1, 2).copy()

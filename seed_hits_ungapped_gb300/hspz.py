@@ -34,7 +34,7 @@ EXPORTS = [
     "hspz_index_free", "hspz_index_info", "hspz_index_tables", "hspz_find_hits", "hspz_plan_free",
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
-    "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed",
+    "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed", "hspz_process_chunk",
 ]
 
 
@@ -93,6 +93,8 @@ def load_library():
         "hspz_compact_noalloc": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_compact_noalloc_max_flags": (U64, []),
         "hspz_score_gate_bucketed": (ctypes.c_int, [VP, VP, VP, U64, P(hspz_score_params), U32, VP, VP]),
+        "hspz_process_chunk": (ctypes.c_int, [VP, U32, P(hspz_score_params), VP, VP, U64, VP, VP, VP, VP, U64,
+                                              P(U64), P(U64), P(ctypes.c_float), VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -300,6 +302,32 @@ def hspz_score_gate_bucketed(index: Index, plan: Plan, d_anchors, n: int, params
                                                  ctypes.byref(params), int(n_buckets),
                                                  _dptr(d_flags, torch.uint8, "d_flags"), _stream(stream))
     _check(rc, "hspz_score_gate_bucketed")
+
+
+def hspz_process_chunk(plan: Plan, chunk: int, params: hspz_score_params, d_anchors, d_flags, d_ids, d_records,
+                       d_done, d_accepted, stream=None, time_gate: bool = False):
+    """One chunk through expansion + gate, compaction, materialization and the
+    accepted compaction, with one host synchronization.  Returns
+    (n_survivors, n_accepted, gate_ms or None); raises HspzError with
+    .needed = n_survivors when the survivor buffers are too small."""
+    import torch
+    cap_a = min(d_anchors.numel() // 2, d_flags.numel())
+    cap_s = min(d_ids.numel(), d_records.numel() // 4, d_done.numel(), d_accepted.numel())
+    ns, na = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    ms = ctypes.c_float(0.0)
+    rc = load_library().hspz_process_chunk(plan.handle, int(chunk), ctypes.byref(params),
+                                           _dptr(d_anchors, torch.int32, "d_anchors"),
+                                           _dptr(d_flags, torch.uint8, "d_flags"), cap_a,
+                                           _dptr(d_ids, torch.int32, "d_ids"), _dptr(d_records, torch.int32, "d_records"),
+                                           _dptr(d_done, torch.uint8, "d_done"),
+                                           _dptr(d_accepted, torch.int32, "d_accepted"), cap_s, ctypes.byref(ns),
+                                           ctypes.byref(na), ctypes.byref(ms) if time_gate else None, _stream(stream))
+    if rc == HSPZ_E_CAPACITY:
+        err = HspzError(rc, "hspz_process_chunk", "needs %d survivor slots" % ns.value)
+        err.needed = ns.value
+        raise err
+    _check(rc, "hspz_process_chunk")
+    return ns.value, na.value, (ms.value if time_gate else None)
 
 
 def hspz_compact(d_flags, n: int, id_base: int, d_ids, stream=None) -> int:

@@ -267,3 +267,34 @@ def test_reference_bucketed_gate_equals_fused(torch_cuda, name, scale):
     bad = hspz.score_params(np.arange(25).reshape(5, 5) - 12, w.xdrop, w.K)  # not complement symmetric
     with pytest.raises(hspz.HspzError):
         hspz.hspz_score_gate_bucketed(eng.index, plan, anchors, n, bad, fused)
+
+
+def test_process_chunk_capacity_and_counts(torch_cuda):
+    """hspz_process_chunk: too little survivor room is reported (anchors and
+    flags written, survivor outputs untouched); with room it matches the
+    oracle's survivors, records and accepted indices."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    w = synth.make("tiny", scale=0.3)
+    eng = _engine(torch, w.ref, w.matrix, w.xdrop, w.K)
+    plan = eng.plan(_dev(torch, w.query))
+    n = plan.total_hits
+    anchors = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+    flags = torch.empty(n, dtype=torch.uint8, device="cuda")
+    small = [torch.full((4,), -3, dtype=torch.int32, device="cuda"), torch.full((4, 4), -3, dtype=torch.int32, device="cuda"),
+             torch.full((4,), 9, dtype=torch.uint8, device="cuda"), torch.full((4,), -3, dtype=torch.int32, device="cuda")]
+    with pytest.raises(hspz.HspzError) as e:
+        hspz.hspz_process_chunk(plan, 0, eng.params, anchors, flags, *small)
+    orc = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K)["per_chunk"][0]
+    assert e.value.needed == orc["ids"].size > 4
+    assert (small[0].cpu().numpy() == -3).all() and (small[2].cpu().numpy() == 9).all()
+    assert np.array_equal(flags.cpu().numpy(), orc["flags"])
+    m = e.value.needed
+    big = [torch.empty(m, dtype=torch.int32, device="cuda"), torch.empty((m, 4), dtype=torch.int32, device="cuda"),
+           torch.empty(m, dtype=torch.uint8, device="cuda"), torch.empty(m, dtype=torch.int32, device="cuda")]
+    ns, na, ms = hspz.hspz_process_chunk(plan, 0, eng.params, anchors, flags, *big, time_gate=True)
+    assert ns == m and na == orc["accepted"].size and ms > 0
+    assert np.array_equal(big[0].cpu().numpy().view(np.uint32), orc["ids"])
+    assert np.array_equal(big[1].cpu().numpy(), orc["rec"])
+    assert np.array_equal(big[2].cpu().numpy(), orc["done"])
+    assert np.array_equal(big[3][:na].cpu().numpy().view(np.uint32), orc["accepted"])
