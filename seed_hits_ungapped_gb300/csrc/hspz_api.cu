@@ -199,10 +199,16 @@ int hspz_build_index(const uint8_t *d_ref, uint64_t ref_len, const char *seed_pa
     cudaError_t e = cudaMalloc((void **)&ix->d_idx, nb * 4);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref, ix->ref_words * 4);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref_rev, ix->ref_words * 4);
-    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 0, ix->d_ref, ix->ref_words, st);
+    unsigned long long *d_ncount = nullptr, ncount = 0;
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&d_ncount, 8, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(d_ncount, 0, 8, st);
+    if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 0, ix->d_ref, ix->ref_words, st, d_ncount);
     if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 1, ix->d_ref_rev, ix->ref_words, st);
     if (e == cudaSuccess) e = build_index_tables(d_ref, ref_len, sh, ix->d_idx, &ix->d_pos, &ix->n_pos, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&ncount, d_ncount, 8, cudaMemcpyDeviceToHost, st);
+    if (d_ncount) cudaFreeAsync(d_ncount, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    ix->has_n = ncount != 0;
     if (e != cudaSuccess) {
         int rc = cuda_fail(e, "hspz_build_index");
         hspz_index_free(ix);
@@ -267,18 +273,23 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     e = cudaMallocAsync((void **)&p->d_P, sa * 4, st);
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_lo, sa * 4, st);
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_cnt, sa * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_blk, (3 * nb + 1) * 8, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_blk, (3 * nb + 2) * 8, st);
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry, p->qry_words * 4, st);
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry_rev, p->qry_words * 4, st);
-    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 0, p->d_qry, p->qry_words, st);
-    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 1, p->d_qry_rev, p->qry_words, st);
+    // the total and the query's N count sit side by side after the block sums
     uint64_t *bsum = p->d_blk, *bexcl = p->d_blk + nb, *bincl = p->d_blk + 2 * nb, *dtot = p->d_blk + 3 * nb;
+    if (e == cudaSuccess) e = cudaMemsetAsync(dtot, 0, 16, st);
+    if (e == cudaSuccess)
+        e = launch_pack(d_query, query_len, 0, 0, p->d_qry, p->qry_words, st, (unsigned long long *)(dtot + 1));
+    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 1, p->d_qry_rev, p->qry_words, st);
     if (e == cudaSuccess && S) e = launch_count(d_query, S, ix->shape, ix->d_idx, p->d_cnt, p->d_lo, bsum, st);
     if (e == cudaSuccess && S) e = launch_scan_u64(bsum, nb, bexcl, bincl, dtot, st);
     if (e == cudaSuccess && S) e = launch_prefix(p->d_cnt, S, bexcl, p->d_P, st);
-    uint64_t total = 0;
-    if (e == cudaSuccess && S) e = cudaMemcpyAsync(&total, dtot, 8, cudaMemcpyDeviceToHost, st);
+    uint64_t tot_n[2] = {0, 0};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(tot_n, dtot, 16, cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    const uint64_t total = tot_n[0];
+    p->has_n = tot_n[1] != 0;
     if (e != cudaSuccess) {
         int rc = cuda_fail(e, "hspz_find_hits");
         hspz_plan_free(p);
@@ -388,7 +399,8 @@ int hspz_expand_gate(const hspz_plan *p, uint32_t chunk, const hspz_score_params
     const uint64_t hits = (uint64_t)c.hit_end - c.hit_begin;
     if (cap < hits) return HSPZ_E_CAPACITY;
     if (hits && (!d_anchors || !d_flags)) return HSPZ_E_INVAL;
-    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev, p->index->has_n},
+        q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = launch_expand_gate(p->d_P, p->d_lo, p->index->d_pos, c, p->index->shape.span, r, q, sa,
                                        d_anchors, d_flags, p->d_tiles, (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_expand_gate");
@@ -415,7 +427,8 @@ int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_para
     uint32_t *scratch = nullptr;
     cudaEvent_t ev0 = nullptr, ev1 = nullptr;
     uint64_t totals[2] = {0, 0};
-    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev, p->index->has_n},
+        q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
     // the two counts sit after the compaction scratch, 8-byte aligned
     uint64_t *tot = reinterpret_cast<uint64_t *>(scratch + ((words - 6) & ~1ull));
@@ -456,7 +469,7 @@ int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor 
     if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags))) return HSPZ_E_INVAL;
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
-    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = launch_gate(d_anchors, nullptr, n, r, q, sa, d_flags, (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate");
 }
@@ -489,7 +502,7 @@ int hspz_score_gate_bucketed(const hspz_index *ix, const hspz_plan *p, const hsp
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&raw, n * 4, st);
     if (e == cudaSuccess) e = cudaMallocAsync((void **)&scratch, bucket_scratch_words(n, n_buckets) * 4, st);
     if (e == cudaSuccess) e = launch_bucket_sort(d_anchors, n, span, n_buckets, sorted, raw, scratch, st);
-    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     if (e == cudaSuccess) e = launch_gate(sorted, raw, n, r, q, sa, d_flags, st);
     for (void *ptr : {(void *)sorted, (void *)raw, (void *)scratch})
         if (ptr) cudaFreeAsync(ptr, st);
@@ -527,7 +540,7 @@ int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor
     if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
-    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev}, q{p->d_qry, p->query_len, p->d_qry_rev};
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done,
                                        (cudaStream_t)stream);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize");

@@ -76,10 +76,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 
 // Scores of one 8-base step, in walk order, as 8 int32 running sums from S.
 // RIGHT: walk order = nibbles 0..7 of the aligned words; left: 7..0.
-template <bool RIGHT>
+template <bool RIGHT, bool HAS_N = true>
 __device__ __forceinline__ void step_sums(uint32_t R, uint32_t Q, uint32_t keep, uint32_t tlo, uint32_t thi,
                                           const int *__restrict__ tab25, int S, int (&Sv)[8]) {
-    const uint32_t nmask = (R | Q) & 0x88888888u & keep;
+    // without N in either sequence only the padding is N, and keep masks it
+    const uint32_t nmask = HAS_N ? ((R | Q) & 0x88888888u & keep) : 0u;
     if (__builtin_expect(nmask == 0, 1)) {
         // masked-off nibbles select entry 0 in sign mode: score 0
         const uint32_t idx = (((R ^ Q) & 0x77777777u) & keep) | (0x88888888u & ~keep);
@@ -272,6 +273,14 @@ __device__ __forceinline__ uint32_t warp_upper_bound(const uint32_t *__restrict_
     return lo + (uint32_t)(__ffs(m) - 1);
 }
 
+// Mask of the low min(n, 8) nibbles (the bases of a step inside the walk).
+__device__ __forceinline__ uint32_t low_nibbles(uint32_t n) {
+    const uint32_t s = min(n, 8u) * 4u;
+    uint32_t d;
+    asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(0xFFFFFFFFu), "r"(s));  // shifts of 32 give 0
+    return ~d;
+}
+
 struct WalkState {
     const uint32_t *pr, *pq;
     uint32_t shr, shq, r0, r1, q0, q1, rem;
@@ -329,17 +338,19 @@ __device__ __forceinline__ void walk_advance(WalkState &w, int S_next) {
 // The common 8-base step.  It advances the walk and returns false unless the
 // step may hold the stop, reaches `need` or ends at the edge; then it leaves
 // the walk untouched and returns true for walk_resolve.
+template <bool HAS_N>
 __device__ __forceinline__ bool walk_step(WalkState &w, uint32_t tlo, uint32_t thi, const int *__restrict__ tab25,
                                           int X, int need, int (&Sv)[8], int &Mb, bool &maybe_stop) {
     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
-    const uint32_t keep = w.rem >= 8 ? 0xFFFFFFFFu : ((1u << (4 * w.rem)) - 1u);
-    step_sums<true>(R, Q, keep, tlo, thi, tab25, w.S, Sv);
+    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
     const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
     const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
     Mb = max(w.M, hi);
-    maybe_stop = lo < Mb - X;
-    if (!(maybe_stop | (Mb >= need) | (w.rem <= 8))) {
+    // sign bits: lo - Mb + X < 0 when the step may hold the stop, need - 1 - Mb < 0 when it reaches need
+    const int gap = lo - Mb + X;
+    maybe_stop = gap < 0;
+    if (!(((gap | (need - 1 - Mb)) < 0) | (w.rem <= 8))) {
         w.M = Mb;
         walk_advance(w, Sv[7]);
         return false;
@@ -403,6 +414,7 @@ __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32
 //      flagged a step that may hold its stop, reaches `need` or ends at the
 //      edge, settle together, then the same for the right side;
 //   3. the warp stores its anchors and flags with coalesced writes.
+template <bool HAS_N>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
     k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
                     const uint32_t *__restrict__ pos, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
@@ -496,7 +508,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
             bool maybe_stop = false;
             while (__any_sync(kFullMask, !ended)) {
                 while (__any_sync(kFullMask, stepping)) {
-                    if (stepping && walk_step(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+                    if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
                 }
                 if (!ended) {
                     bool acc = false;
@@ -521,6 +533,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
 // sorted by reference window with their raw ids).  One warp per unit of 256
 // anchors, 8 synchronous rounds of 32 as in k_expand_gate_w; the flag of
 // anchor i goes to flags[raw ? raw[i] : i].
+template <bool HAS_N>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
     k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq,
                   const uint32_t *__restrict__ ref_rev, const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
@@ -559,7 +572,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
                 bool maybe_stop = false;
                 while (__any_sync(kFullMask, !ended)) {
                     while (__any_sync(kFullMask, stepping)) {
-                        if (stepping && walk_step(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+                        if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
                     }
                     if (!ended) {
                         bool acc = false;
@@ -617,6 +630,7 @@ __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict_
 // step's start; when the side ends that one step is scored again to find the
 // exact base (E.2 invariant).  A side that passes 2^20 steps (|S| could then
 // approach 2^31) sends the survivor to the 64-bit base-by-base walk.
+template <bool HAS_N>
 __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                           uint32_t id_base, const uint32_t *__restrict__ ids,
                                                           uint64_t n_ids, const uint64_t *__restrict__ d_n, Seqs sq,
@@ -653,9 +667,8 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
                 for (;;) {
                     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
                     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
-                    const uint32_t keep = w.rem >= 8 ? 0xFFFFFFFFu : ((1u << (4 * w.rem)) - 1u);
                     int Sv[8];
-                    step_sums<true>(R, Q, keep, tlo, thi, tab, w.S, Sv);
+                    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab, w.S, Sv);
                     const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])),
                                        max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
                     const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])),
@@ -709,7 +722,7 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
                         const uint32_t back = steps - (uint32_t)mstep;
                         const uint32_t *pr = w.pr - back, *pq = w.pq - back;
                         int Sm[8];
-                        step_sums<true>(__funnelshift_r(__ldg(pr), __ldg(pr + 1), w.shr),
+                        step_sums<true, HAS_N>(__funnelshift_r(__ldg(pr), __ldg(pr + 1), w.shr),
                                         __funnelshift_r(__ldg(pq), __ldg(pq + 1), w.shq), 0xFFFFFFFFu, tlo, thi,
                                         tab, mS, Sm);
                         int kk = 7;
@@ -814,9 +827,13 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
     } else if (sa.fast) {
         const uint64_t n_tiles = (n + kWTile - 1) / kWTile;
         k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
-        k_expand_gate_w<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span,
-                                                                    seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa,
-                                                                    out, d_flags); count_launch();
+        if (ref.has_n || qry.has_n) {
+            k_expand_gate_w<true><<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(
+                d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa, out, d_flags); count_launch();
+        } else {
+            k_expand_gate_w<false><<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(
+                d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa, out, d_flags); count_launch();
+        }
     } else {
         k_expand_gate<true><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     }
@@ -829,8 +846,13 @@ cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uin
     if (sa.fast) {
         const uint64_t units = (n + kWUnit - 1) / kWUnit, want = (units + kWWarps - 1) / kWWarps;
         const unsigned g = (unsigned)(want < 152ull * 40 ? want : 152ull * 40);
-        k_gate_rounds<<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n, seqs(ref, qry),
-                                                   ref.rev, qry.rev, sa, d_flags); count_launch();
+        if (ref.has_n || qry.has_n) {
+            k_gate_rounds<true><<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n,
+                                                             seqs(ref, qry), ref.rev, qry.rev, sa, d_flags); count_launch();
+        } else {
+            k_gate_rounds<false><<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n,
+                                                              seqs(ref, qry), ref.rev, qry.rev, sa, d_flags); count_launch();
+        }
     } else if (!d_raw) {
         k_gate<false><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
                                                          d_flags); count_launch();
@@ -849,8 +871,14 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
     uint4 *out = reinterpret_cast<uint4 *>(d_out);
     if (sa.fast) {
         const uint64_t blocks = (n_ids + 255) / 256;
-        k_materialize_lane<<<(unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64), 256, 0, st>>>(
-            an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa, out, d_done); count_launch();
+        const unsigned g = (unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64);
+        if (ref.has_n || qry.has_n) {
+            k_materialize_lane<true><<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry),
+                                                        ref.rev, qry.rev, sa, out, d_done); count_launch();
+        } else {
+            k_materialize_lane<false><<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry),
+                                                         ref.rev, qry.rev, sa, out, d_done); count_launch();
+        }
     } else {
         k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry),
                                                                     sa, out, d_done); count_launch();

@@ -15,7 +15,8 @@ __device__ __forceinline__ uint32_t pack_nibble(uint32_t c, int parity) {
 
 // One thread per packed word: 8 bases, padded with N outside [0, len).
 __global__ void k_pack(const uint8_t *__restrict__ codes, uint64_t len, int parity, int reverse,
-                       uint32_t *__restrict__ out, uint64_t words) {
+                       uint32_t *__restrict__ out, uint64_t words, unsigned long long *__restrict__ n_count) {
+    unsigned long long ns = 0;
     for (uint64_t w = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; w < words;
          w += (uint64_t)gridDim.x * blockDim.x) {
         int64_t b0 = (int64_t)w * 8 - kPadBases;
@@ -24,11 +25,15 @@ __global__ void k_pack(const uint8_t *__restrict__ codes, uint64_t len, int pari
         for (int i = 0; i < 8; i++) {
             int64_t b = b0 + i;
             uint32_t nib = kNibN;
-            if (b >= 0 && (uint64_t)b < len) nib = pack_nibble(codes[reverse ? len - 1 - b : b], parity);
+            if (b >= 0 && (uint64_t)b < len) {
+                nib = pack_nibble(codes[reverse ? len - 1 - b : b], parity);
+                ns += nib == kNibN;
+            }
             v |= nib << (4 * i);
         }
         out[w] = v;
     }
+    if (n_count && ns) atomicAdd(n_count, ns);
 }
 
 template <typename T>
@@ -288,8 +293,8 @@ uint64_t packed_words(uint64_t len) {
 }
 
 cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, int reverse, uint32_t *d_packed,
-                        uint64_t words, cudaStream_t st) {
-    k_pack<<<grid_for(words, 256), 256, 0, st>>>(d_codes, len, with_parity, reverse, d_packed, words); count_launch();
+                        uint64_t words, cudaStream_t st, unsigned long long *d_n_count) {
+    k_pack<<<grid_for(words, 256), 256, 0, st>>>(d_codes, len, with_parity, reverse, d_packed, words, d_n_count); count_launch();
     return cudaGetLastError();
 }
 

@@ -44,6 +44,7 @@ struct SeqView {
     const uint32_t *packed;  // padded packed words
     uint64_t len;            // bases
     const uint32_t *rev;     // padded packed words of the reversed sequence (base i = base len-1-i)
+    bool has_n;              // some base is N (not A/C/G/T)
 };
 
 int parse_pattern(const char *pat, SeedShape *sh);
@@ -63,8 +64,9 @@ int cuda_fail(cudaError_t e, const char *what);
     } while (0)
 
 // launchers (each returns cudaError_t of the launch)
+// d_n_count (nullable) is incremented by the number of N bases packed
 cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, int reverse, uint32_t *d_packed,
-                        uint64_t words, cudaStream_t st);
+                        uint64_t words, cudaStream_t st, unsigned long long *d_n_count = nullptr);
 cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedShape &sh, const uint32_t *d_idx,
                          uint32_t *d_cnt, uint32_t *d_lo, uint64_t *d_block_sum, cudaStream_t st);
 cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, uint64_t *d_incl,
@@ -110,6 +112,7 @@ struct hspz_index {
     uint32_t *d_ref_rev;  // packed reversed reference (left walks run forward over it)
     uint64_t ref_words;
     int device;
+    bool has_n;            // the reference holds N
 };
 
 struct hspz_plan {
@@ -124,6 +127,7 @@ struct hspz_plan {
     uint64_t n_blocks;
     uint32_t *d_qry;        // packed query
     uint32_t *d_qry_rev;    // packed reversed query
+    bool has_n;             // the query holds N
     uint64_t qry_words;
     std::vector<hspz_chunk> chunks;
     uint64_t max_chunk_hits;
