@@ -313,13 +313,10 @@ def main():
             d2h = 0
             for pq in pinned:
                 dq = pq.to("cuda", non_blocking=True)
-                res = eng.run(dq, max_hits=w.max_hits)
-                # the step's result: accepted records, done flags and accepted ids to host
+                # the step's result, chunk by chunk: records, done flags and accepted ids to host
+                res = eng.run(dq, max_hits=w.max_hits, fetch=True)
                 for c in res.per_chunk:
-                    rec = eng._bufs["records"][: c.n_survivors].cpu()
-                    dn = eng._bufs["done"][: c.n_survivors].cpu()
-                    acc = eng._bufs["accepted"][: c.n_accepted].cpu()
-                    d2h += rec.numel() * 4 + dn.numel() + acc.numel() * 4
+                    d2h += c.records.nbytes + c.done.nbytes + c.accepted.nbytes
             torch.cuda.synchronize()
             if it >= args.warmup:
                 e2e_ms.append(1e3 * (time.perf_counter() - t0))
@@ -334,14 +331,18 @@ def main():
         dist.destroy_process_group()
     if rank != 0:
         return 0
-    res = eng.run(d_queries[0], max_hits=w.max_hits)
+    # survivor, accepted and chunk counts over every query batch of one step
+    results = [eng.run(dq, max_hits=w.max_hits) for dq in d_queries]
+    n_surv_step = sum(r.n_survivors for r in results)
+    n_acc_step = sum(r.n_accepted for r in results)
+    n_chunks_step = sum(len(r.chunks) for r in results)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
         "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload), "anchors_per_step": n_anchors,
-                   "seeds_per_step": n_seeds, "survivors": res.n_survivors, "accepted": res.n_accepted,
-                   "chunks": int(len(res.chunks)), "l2": "flushed (512 MiB write) between timed steps",
+                   "seeds_per_step": n_seeds, "survivors": n_surv_step, "accepted": n_acc_step,
+                   "chunks": n_chunks_step, "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "expand_gate_anchors_per_s": n_anchors * args.steps / (sum(gate_ms) / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

@@ -98,6 +98,12 @@ int make_score_args(const hspz_score_params *p, ScoreArgs *out) {
     out->tab_hi = (uint8_t)tab[4] | ((uint32_t)(uint8_t)tab[5] << 8) | ((uint32_t)(uint8_t)tab[6] << 16) |
                   ((uint32_t)(uint8_t)tab[7] << 24);
     out->fast = fast ? 1 : 0;
+    // After a stop inside an 8-base step, at most 7 more pair scores follow in
+    // that step; they cannot lift the running sum back above the maximum
+    // before the stop when X is at least 7 times the largest pair score.
+    int smax = 0;
+    for (int i = 0; i < 25; i++) smax = p->matrix[i] > smax ? p->matrix[i] : smax;
+    out->exact = (fast && (int64_t)p->xdrop >= 7 * (int64_t)smax) ? 1 : 0;
     return HSPZ_OK;
 }
 

@@ -253,26 +253,6 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
 // ------------------------------------------------------------------ warp helpers for the fused fast kernel
 constexpr unsigned kFullMask = 0xFFFFFFFFu;
 
-// First s in [lo, hi) with P[s] > key (hi if none); called by a whole warp.
-__device__ __forceinline__ uint32_t warp_upper_bound(const uint32_t *__restrict__ P, uint32_t lo, uint32_t hi,
-                                                     uint32_t key, int lane) {
-    while (hi - lo > 31) {
-        const uint32_t span = hi - lo;
-        const uint32_t probe = lo + (uint32_t)(((uint64_t)span * (uint32_t)(lane + 1)) / 33u);
-        const unsigned m = __ballot_sync(kFullMask, __ldg(P + probe) > key);
-        const int f = m ? __ffs(m) - 1 : 32;
-        const uint32_t below = __shfl_sync(kFullMask, probe, f > 0 ? f - 1 : 0);
-        const uint32_t above = __shfl_sync(kFullMask, probe, f < 32 ? f : 31);
-        const uint32_t nlo = f == 0 ? lo : below + 1;
-        const uint32_t nhi = f == 32 ? hi : above;
-        lo = nlo;
-        hi = nhi;
-    }
-    const uint32_t idx = lo + (uint32_t)lane;
-    const unsigned m = __ballot_sync(kFullMask, idx >= hi || __ldg(P + idx) > key);
-    return lo + (uint32_t)(__ffs(m) - 1);
-}
-
 // Mask of the low min(n, 8) nibbles (the bases of a step inside the walk).
 __device__ __forceinline__ uint32_t low_nibbles(uint32_t n) {
     const uint32_t s = min(n, 8u) * 4u;
@@ -299,27 +279,6 @@ __device__ __forceinline__ void walk_place(WalkState &w, const Seqs &sq, const u
     w.pq = (side ? sq.qry : qry_rev) + (jq >> 3);
     w.shr = (jr & 7u) * 4u;
     w.shq = (jq & 7u) * 4u;
-    w.S = 0;
-    w.M = 0;
-}
-
-// Start one side of anchor (ar, aq): side 0 walks left (forward over the
-// reversed sequences from the base before the anchor), side 1 walks right.
-__device__ __forceinline__ void walk_start(WalkState &w, const Seqs &sq, const uint32_t *ref_rev,
-                                           const uint32_t *qry_rev, uint32_t ar, uint32_t aq, int side) {
-    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
-    const uint32_t rb = side ? ar : Lr - ar;
-    const uint32_t qb = side ? aq : Lq - aq;
-    w.rem = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
-    const uint32_t jr = rb + (uint32_t)kPadBases, jq = qb + (uint32_t)kPadBases;
-    w.pr = (side ? sq.ref : ref_rev) + (jr >> 3);
-    w.pq = (side ? sq.qry : qry_rev) + (jq >> 3);
-    w.shr = (jr & 7u) * 4u;
-    w.shq = (jq & 7u) * 4u;
-    w.r0 = __ldg(w.pr);
-    w.r1 = __ldg(w.pr + 1);
-    w.q0 = __ldg(w.pq);
-    w.q1 = __ldg(w.pq + 1);
     w.S = 0;
     w.M = 0;
 }
@@ -387,6 +346,103 @@ __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], i
     return false;
 }
 
+// The 8-base step with an exact stop test, for scoring where X >= 7 * the
+// largest single-pair score (and X >= 0).  Base k of the step stops the walk
+// when it falls more than X below the running maximum m(k-1) of the bases
+// before it.  After such a stop the remaining (at most 7) sums of the step
+// cannot climb back above m(k-1), so the step's final running maximum is the
+// side maximum at the stop: the step never has to be replayed base by base.
+// Returns true when the side is over (stop, `need` reached or edge) with
+// w.M = the side maximum; otherwise the walk has advanced.
+template <bool HAS_N>
+__device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint32_t thi,
+                                                const int *__restrict__ tab25, int X, int need) {
+    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
+    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
+    int Sv[8];
+    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
+    // d collects the sign of S(k) + X - m(k-1) for every base k
+    int m = w.M, d = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        d |= Sv[k] + X - m;
+        m = max(m, Sv[k]);
+    }
+    w.M = m;
+    if (((d | (need - 1 - m)) < 0) | (w.rem <= 8)) return true;
+    walk_advance(w, Sv[7]);
+    return false;
+}
+
+// One synchronous round of 32 anchors, one per lane (`walk0` false for an
+// empty slot): all lanes start their left side together, step until every
+// lane's side is over, then do the right side the same way.  The right
+// side's first words are loaded with the left side's.  EXACT selects
+// walk_step_exact; otherwise flagged steps are settled by walk_resolve,
+// together, after every lane has flagged.  Returns the keep decision.
+template <bool HAS_N, bool EXACT>
+__device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, const uint32_t *__restrict__ ref_rev,
+                                           const uint32_t *__restrict__ qry_rev, uint32_t tlo, uint32_t thi,
+                                           const int *__restrict__ tab, int X, int T) {
+    bool accepted = false;
+    int need = T;
+    uint32_t nr0 = 0, nr1 = 0, nq0 = 0, nq1 = 0;  // the right side's first words
+#pragma unroll 1
+    for (int side = 0; side < 2; side++) {
+        const bool walk = walk0 && !accepted;
+        WalkState w;
+        if (walk) {
+            walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
+            if (side == 0) {  // the left side's first words, and the right side's, in one go
+                w.r0 = __ldg(w.pr);
+                w.r1 = __ldg(w.pr + 1);
+                w.q0 = __ldg(w.pq);
+                w.q1 = __ldg(w.pq + 1);
+                const uint32_t jr = a.x + (uint32_t)kPadBases, jq = a.y + (uint32_t)kPadBases;
+                nr0 = __ldg(sq.ref + (jr >> 3));
+                nr1 = __ldg(sq.ref + (jr >> 3) + 1);
+                nq0 = __ldg(sq.qry + (jq >> 3));
+                nq1 = __ldg(sq.qry + (jq >> 3) + 1);
+            } else {
+                w.r0 = nr0;
+                w.r1 = nr1;
+                w.q0 = nq0;
+                w.q1 = nq1;
+            }
+        }
+        bool stepping = walk;
+        if (EXACT) {
+            while (__any_sync(kFullMask, stepping)) {
+                if (stepping && walk_step_exact<HAS_N>(w, tlo, thi, tab, X, need)) stepping = false;
+            }
+            if (walk) {
+                accepted = w.M >= need;
+                need = T - w.M;
+            }
+        } else {
+            bool ended = !walk;
+            int Sv[8], Mb = 0;
+            bool maybe_stop = false;
+            while (__any_sync(kFullMask, !ended)) {
+                while (__any_sync(kFullMask, stepping)) {
+                    if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+                }
+                if (!ended) {
+                    bool acc = false;
+                    if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
+                        ended = true;
+                        accepted = acc;
+                        need = T - w.M;
+                    } else {
+                        stepping = true;
+                    }
+                }
+            }
+        }
+    }
+    return accepted;
+}
+
 constexpr int kWWarps = 8;             // warps per CTA
 constexpr int kWUnit = 256;            // anchor slots per warp
 constexpr int kWTile = kWWarps * kWUnit;
@@ -414,7 +470,7 @@ __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32
 //      flagged a step that may hold its stop, reaches `need` or ends at the
 //      edge, settle together, then the same for the right side;
 //   3. the warp stores its anchors and flags with coalesced writes.
-template <bool HAS_N>
+template <bool HAS_N, bool EXACT>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
     k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
                     const uint32_t *__restrict__ pos, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
@@ -477,51 +533,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
         const bool valid = ai < count;
         uint2 a = make_uint2(0, 0);
         if (valid) a = sA[ai];
-        bool accepted = false;
-        int need = T;
-        uint32_t nr0 = 0, nr1 = 0, nq0 = 0, nq1 = 0;  // the right side's first words
-#pragma unroll 1
-        for (int side = 0; side < 2; side++) {
-            const bool walk = valid && !accepted;
-            WalkState w;
-            if (walk) {
-                walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
-                if (side == 0) {  // the left side's first words, and the right side's, in one go
-                    w.r0 = __ldg(w.pr);
-                    w.r1 = __ldg(w.pr + 1);
-                    w.q0 = __ldg(w.pq);
-                    w.q1 = __ldg(w.pq + 1);
-                    const uint32_t jr = a.x + (uint32_t)kPadBases, jq = a.y + (uint32_t)kPadBases;
-                    nr0 = __ldg(sq.ref + (jr >> 3));
-                    nr1 = __ldg(sq.ref + (jr >> 3) + 1);
-                    nq0 = __ldg(sq.qry + (jq >> 3));
-                    nq1 = __ldg(sq.qry + (jq >> 3) + 1);
-                } else {
-                    w.r0 = nr0;
-                    w.r1 = nr1;
-                    w.q0 = nq0;
-                    w.q1 = nq1;
-                }
-            }
-            bool ended = !walk, stepping = walk;
-            int Sv[8], Mb = 0;
-            bool maybe_stop = false;
-            while (__any_sync(kFullMask, !ended)) {
-                while (__any_sync(kFullMask, stepping)) {
-                    if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
-                }
-                if (!ended) {
-                    bool acc = false;
-                    if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
-                        ended = true;
-                        accepted = acc;
-                        if (side == 0) need = T - w.M;
-                    } else {
-                        stepping = true;
-                    }
-                }
-            }
-        }
+        const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, ref_rev, qry_rev, tlo, thi, tab, X, T);
         if (valid) flags[t0 + ai] = accepted ? 1 : 0;
     }
     // 3. anchors
@@ -533,7 +545,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
 // sorted by reference window with their raw ids).  One warp per unit of 256
 // anchors, 8 synchronous rounds of 32 as in k_expand_gate_w; the flag of
 // anchor i goes to flags[raw ? raw[i] : i].
-template <bool HAS_N>
+template <bool HAS_N, bool EXACT>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
     k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq,
                   const uint32_t *__restrict__ ref_rev, const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
@@ -554,38 +566,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
             uint2 a = make_uint2(0, 0);
             if (valid) a = anchors[t0 + ai];
             const bool inside = valid && a.x < sq.Lr && a.y < sq.Lq;
-            bool accepted = false;
-            int need = T;
-#pragma unroll 1
-            for (int side = 0; side < 2; side++) {
-                const bool walk = inside && !accepted;
-                WalkState w;
-                if (walk) {
-                    walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
-                    w.r0 = __ldg(w.pr);
-                    w.r1 = __ldg(w.pr + 1);
-                    w.q0 = __ldg(w.pq);
-                    w.q1 = __ldg(w.pq + 1);
-                }
-                bool ended = !walk, stepping = walk;
-                int Sv[8], Mb = 0;
-                bool maybe_stop = false;
-                while (__any_sync(kFullMask, !ended)) {
-                    while (__any_sync(kFullMask, stepping)) {
-                        if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
-                    }
-                    if (!ended) {
-                        bool acc = false;
-                        if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
-                            ended = true;
-                            accepted = acc;
-                            if (side == 0) need = T - w.M;
-                        } else {
-                            stepping = true;
-                        }
-                    }
-                }
-            }
+            const bool accepted = gate_round<HAS_N, EXACT>(a, inside, sq, ref_rev, qry_rev, tlo, thi, tab, X, T);
             if (valid) flags[raw ? raw[t0 + ai] : t0 + ai] = accepted ? 1 : 0;
         }
     }
@@ -827,13 +808,10 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
     } else if (sa.fast) {
         const uint64_t n_tiles = (n + kWTile - 1) / kWTile;
         k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
-        if (ref.has_n || qry.has_n) {
-            k_expand_gate_w<true><<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(
-                d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa, out, d_flags); count_launch();
-        } else {
-            k_expand_gate_w<false><<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(
-                d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev, qry.rev, d_tiles, sa, out, d_flags); count_launch();
-        }
+        auto kern = sa.exact ? (ref.has_n || qry.has_n ? k_expand_gate_w<true, true> : k_expand_gate_w<false, true>)
+                             : (ref.has_n || qry.has_n ? k_expand_gate_w<true, false> : k_expand_gate_w<false, false>);
+        kern<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev,
+                                                         qry.rev, d_tiles, sa, out, d_flags); count_launch();
     } else {
         k_expand_gate<true><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     }
@@ -846,13 +824,10 @@ cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uin
     if (sa.fast) {
         const uint64_t units = (n + kWUnit - 1) / kWUnit, want = (units + kWWarps - 1) / kWWarps;
         const unsigned g = (unsigned)(want < 152ull * 40 ? want : 152ull * 40);
-        if (ref.has_n || qry.has_n) {
-            k_gate_rounds<true><<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n,
-                                                             seqs(ref, qry), ref.rev, qry.rev, sa, d_flags); count_launch();
-        } else {
-            k_gate_rounds<false><<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n,
-                                                              seqs(ref, qry), ref.rev, qry.rev, sa, d_flags); count_launch();
-        }
+        auto kern = sa.exact ? (ref.has_n || qry.has_n ? k_gate_rounds<true, true> : k_gate_rounds<false, true>)
+                             : (ref.has_n || qry.has_n ? k_gate_rounds<true, false> : k_gate_rounds<false, false>);
+        kern<<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n, seqs(ref, qry), ref.rev,
+                                         qry.rev, sa, d_flags); count_launch();
     } else if (!d_raw) {
         k_gate<false><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
                                                          d_flags); count_launch();

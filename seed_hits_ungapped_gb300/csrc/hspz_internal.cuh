@@ -38,6 +38,7 @@ struct ScoreArgs {
     // complement-symmetric int8 table for the fast gate: entry (r ^ q) | parity(r) << 2
     uint32_t tab_lo, tab_hi;
     int fast;  // 1 when the fast table reproduces m exactly on A/C/G/T
+    int exact; // 1 when fast and X >= 7 * max(0, largest entry of m): the gate's 8-base step needs no replay
 };
 
 struct SeqView {

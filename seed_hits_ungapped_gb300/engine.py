@@ -116,7 +116,11 @@ class HspEngine:
                     raise
                 cap = int(e.needed * 1.1) + 1024
 
-    def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False) -> BatchResult:
+    def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False,
+            fetch: bool = False) -> BatchResult:
+        """The whole path over one query batch.  keep=True copies every
+        intermediate of every chunk to host; fetch=True copies only the
+        results (records, done flags, accepted ids) of every chunk."""
         plan = self.plan(d_query, max_hits, walk_full)
         out = []
         for c in range(plan.n_chunks):
@@ -132,6 +136,10 @@ class HspEngine:
                 r.records = rec[:n_surv].cpu().numpy().copy()
                 r.done = done[:n_surv].cpu().numpy().copy()
                 r.accepted = _np_u32(acc[:n_acc]).copy()
+            elif fetch:
+                r.records = rec[:n_surv].cpu().numpy()
+                r.done = done[:n_surv].cpu().numpy()
+                r.accepted = _np_u32(acc[:n_acc])
             out.append(r)
         res = BatchResult(plan.n_seeds, plan.total_hits, plan.chunks.copy(), out)
         if keep:

@@ -120,6 +120,21 @@ def test_chunk_walk_modes_agree(torch_cuda):
     assert_same_as_oracle(a, orc)
 
 
+def test_run_fetch_returns_every_chunk(torch_cuda):
+    """fetch=True (the results-only copy the end-to-end timing uses) hands
+    back each chunk's own records, done flags and accepted ids."""
+    w = synth.make("chunking", scale=0.02)
+    eng = _engine(torch_cuda, w.ref, w.matrix, w.xdrop, w.K)
+    got = eng.run(_dev(torch_cuda, w.query), max_hits=w.max_hits, fetch=True)
+    orc = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K, max_hits=w.max_hits)
+    assert len(got.per_chunk) == len(orc["per_chunk"]) > 3
+    for g, o in zip(got.per_chunk, orc["per_chunk"]):
+        assert g.anchors is None and g.flags is None
+        assert np.array_equal(g.records, o["rec"])
+        assert np.array_equal(g.done, o["done"])
+        assert np.array_equal(g.accepted, o["accepted"])
+
+
 @pytest.mark.parametrize("xdrop,K", [(0, 1), (50, 200), (910, 3000), (1 << 30, 5000)])
 def test_general_matrix(torch_cuda, xdrop, K):
     """An asymmetric random matrix (not complement-symmetric) and extreme X/K."""
@@ -129,6 +144,27 @@ def test_general_matrix(torch_cuda, xdrop, K):
     w = synth.make("tiny", scale=0.2)
     gpu, orc = run_both(torch_cuda, w.ref, w.query, m, xdrop, K)
     assert_same_as_oracle(gpu, orc)
+
+
+@pytest.mark.parametrize("xdrop,K", [(0, 1), (150, 600), (699, 2000), (700, 2000), (910, 3000), (910, 800)])
+@pytest.mark.parametrize("name,scale", [("tiny", 0.2), ("mid", 0.02)])
+def test_fast_gate_both_step_tests(torch_cuda, name, scale, xdrop, K):
+    """HOXD70 (largest pair score 100) on both sides of X = 7 * 100: below it
+    the 8-base step flags possible stops and replays them base by base, from
+    it up the step's stop test is exact.  mid holds N runs."""
+    w = synth.make(name, scale=scale)
+    gpu, orc = run_both(torch_cuda, w.ref, w.query, w.matrix, xdrop, K)
+    assert_same_as_oracle(gpu, orc)
+    # the standalone round gate on the same anchors
+    from seed_hits_ungapped_gb300 import hspz
+    eng = _engine(torch_cuda, w.ref, w.matrix, xdrop, K)
+    plan = eng.plan(_dev(torch_cuda, w.query))
+    for g in gpu.per_chunk:
+        anchors = torch_cuda.from_numpy(g.anchors.view(np.int32)).cuda()
+        flags = torch_cuda.zeros(len(g.anchors), dtype=torch_cuda.uint8, device="cuda")
+        hspz.hspz_score_gate(eng.index, plan, anchors, len(g.anchors), eng.params, flags)
+        assert np.array_equal(flags.cpu().numpy(), g.flags)
+    plan.close()
 
 
 def test_edges(torch_cuda):
