@@ -74,6 +74,8 @@ def _load():
             lib.orc_compact.restype = U64
             lib.orc_materialize.argtypes = [P, U64, P, U64, P, ctypes.c_uint32, P, U64, P, I32, I32, P, P]
             lib.orc_materialize.restype = None
+            lib.orc_dedup.argtypes = [P, U64, P]
+            lib.orc_dedup.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -238,12 +240,26 @@ def materialize(ref, qry, anchors, id_base: int, ids, matrix, xdrop: int, T: int
     return rec, done
 
 
+def dedup(records):
+    """keep (n,) uint8: 1 for the first record, in the given order, of every
+    group of records equal in all four fields (see orc_dedup)."""
+    rec = np.ascontiguousarray(records, dtype=np.int32).reshape(-1, 4)
+    keep = np.zeros(rec.shape[0], dtype=np.uint8)
+    if rec.shape[0]:
+        rc = _load().orc_dedup(_p(rec), rec.shape[0], _p(keep))
+        if rc:
+            raise OracleError("orc_dedup failed (%d)" % rc)
+    return keep
+
+
 def run_path(ref, qry, matrix, xdrop: int, K: int, max_hits: int = 0, pattern: str = SEED_PATTERN,
              index=None):
     """The whole path for one query batch, step by step (small inputs only).
 
     Returns a dict with buckets, counts, P, total, rc, chunks and, per chunk,
-    anchors, flags, survivor ids, records and done flags.
+    anchors, flags, survivor ids, records and done flags; then the accepted
+    records of the batch in raw order ("accepted_rec") and the ones kept by
+    dedup ("final_idx" into accepted_rec, "final_rec").
     """
     _, span = pattern_info(pattern)
     idx, pos = index if index is not None else build_index(ref, pattern)
@@ -264,4 +280,10 @@ def run_path(ref, qry, matrix, xdrop: int, K: int, max_hits: int = 0, pattern: s
         rec, done = materialize(ref, qry, anchors, int(c[2]), ids, matrix, xdrop, T)
         acc = compact(done, 0)
         res["per_chunk"].append(dict(anchors=anchors, flags=flags, ids=ids, rec=rec, done=done, accepted=acc))
+    parts = [pc["rec"][pc["accepted"]] for pc in res["per_chunk"]]
+    accepted_rec = np.concatenate(parts) if parts else np.zeros((0, 4), np.int32)
+    keep = dedup(accepted_rec)
+    res["accepted_rec"] = accepted_rec
+    res["final_idx"] = np.flatnonzero(keep).astype(np.uint32)
+    res["final_rec"] = accepted_rec[keep.astype(bool)]
     return res

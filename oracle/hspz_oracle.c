@@ -374,3 +374,48 @@ void orc_materialize(const uint8_t *ref, uint64_t ref_len, const uint8_t *qry, u
         }
     }
 }
+
+/* ---------------------------------------------------------------------------
+ * Duplicate removal over the accepted HSPs of one query batch ("D. Score
+ * gate": the accepted raw HSPs become the final HSPs after dedup; "C. Hit
+ * discovery" C.5: the raw anchor order fixes the dedup scope).  The pages do
+ * not state the criterion; the reading taken here: a record is dropped when
+ * an earlier record of the batch, in raw order, has the same four fields
+ * (ref_start, query_start, len, score).  keep[i] = 1 for the first of every
+ * group of equal records.  Method: sort the indices by (record, index) with
+ * qsort; the first index of each run of equal records is the one kept.
+ * PARITY OF THE CRITERION IS UNPINNED (the pages give only the funnel counts);
+ * the function itself is pinned to that reading by brute force.
+ * ------------------------------------------------------------------------- */
+static const int32_t *dedup_rec;
+
+static int dedup_cmp(const void *pa, const void *pb)
+{
+    uint64_t a = *(const uint64_t *)pa, b = *(const uint64_t *)pb;
+    for (int f = 0; f < 4; f++) {
+        int32_t x = dedup_rec[4 * a + f], y = dedup_rec[4 * b + f];
+        if (x != y) return x < y ? -1 : 1;
+    }
+    return a < b ? -1 : (a > b ? 1 : 0);
+}
+
+int orc_dedup(const int32_t *rec, uint64_t n, uint8_t *keep)
+{
+    if (n == 0) return ORC_OK;
+    uint64_t *order = (uint64_t *)malloc(n * sizeof(uint64_t));
+    if (!order) return ORC_E_INVAL;
+    for (uint64_t i = 0; i < n; i++) order[i] = i;
+    dedup_rec = rec;
+    qsort(order, n, sizeof(uint64_t), dedup_cmp);
+    for (uint64_t k = 0; k < n; k++) {
+        uint64_t i = order[k];
+        int first = 1;
+        if (k > 0) {
+            uint64_t j = order[k - 1];
+            first = memcmp(rec + 4 * i, rec + 4 * j, 4 * sizeof(int32_t)) != 0;
+        }
+        keep[i] = (uint8_t)first;
+    }
+    free(order);
+    return ORC_OK;
+}

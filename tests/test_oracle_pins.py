@@ -355,3 +355,54 @@ def test_materialized_records_score_their_closed_interval():
             assert ln + 1 == sides[k, 1] + sides[k, 3]
             seen += 1
     assert seen > 100
+
+
+# ---------------------------------------------------------------- dedup (criterion: reading, parity unpinned)
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_dedup_equals_pairwise_brute_force(seed):
+    """keep[i] = 1 iff no earlier record equals record i in all four fields."""
+    rng = np.random.default_rng(seed)
+    n = 400
+    rec = rng.integers(-2, 3, (n, 4)).astype(np.int32)
+    rec[rng.random(n) < 0.1] = [np.iinfo(np.int32).min, np.iinfo(np.int32).max, 0, -1]
+    keep = oracle.dedup(rec)
+    for i in range(n):
+        earlier = any((rec[j] == rec[i]).all() for j in range(i))
+        assert keep[i] == (0 if earlier else 1)
+
+
+def test_dedup_properties_and_edges():
+    rng = np.random.default_rng(5)
+    rec = rng.integers(0, 4, (5000, 4)).astype(np.int32)
+    keep = oracle.dedup(rec).astype(bool)
+    kept = rec[keep]
+    # as many kept as there are distinct rows, all distinct, first occurrences
+    assert kept.shape[0] == np.unique(rec, axis=0).shape[0]
+    assert np.unique(kept, axis=0).shape[0] == kept.shape[0]
+    _, first = np.unique(rec, axis=0, return_index=True)
+    assert np.array_equal(np.sort(first), np.flatnonzero(keep))
+    # records that differ in one field only, in the sign of a field, or not at all
+    r = np.array([[1, 2, 3, 4], [1, 2, 3, -4], [1, 2, 3, 4], [0, 2, 3, 4], [1, 2, 3, 4]], np.int32)
+    assert oracle.dedup(r).tolist() == [1, 1, 0, 1, 0]
+    assert oracle.dedup(np.zeros((0, 4), np.int32)).size == 0
+    assert oracle.dedup(np.ones((7, 4), np.int32)).tolist() == [1, 0, 0, 0, 0, 0, 0]
+
+
+def test_dedup_leaves_one_hsp_per_exact_copy():
+    """A query holding an exact 300 bp copy of the reference between N runs:
+    every seed hit on that diagonal extends over the whole copy (all pair
+    scores positive, the N flanks stop both sides after 10 bases), so all the
+    accepted records are equal and dedup keeps exactly the first one, with
+    the closed-form score of the copy."""
+    rng = np.random.default_rng(21)
+    m = hoxd70()
+    ref = rng.integers(0, 4, 20_000).astype(np.uint8)
+    seg = ref[7_000:7_300]
+    qry = np.concatenate([np.full(50, 4, np.uint8), seg, np.full(50, 4, np.uint8)])
+    res = oracle.run_path(ref, qry, m, 910, 3000)
+    acc = res["accepted_rec"]
+    assert acc.shape[0] > 100
+    score = sum(DIAG_HOXD70[int(b)] for b in seg)
+    assert res["final_rec"].tolist() == [[7_000, 50, 299, score]]
+    assert res["final_idx"].tolist() == [0]
