@@ -4,7 +4,10 @@ One step = the whole path over one synthetic query batch: hit discovery
 (count, prefix, chunk walk), fused expansion + score gate, stable compaction,
 materialization and the accepted compaction.  The metric is anchors per
 second; the dominant kernel (fused expansion + gate) is also reported against
-the HBM roofline.
+the HBM roofline ("roofline") and, from ncu instruction counts of the same
+kernel version, against the SMs' instruction issue rate ("issue_roofline").
+Duplicate removal over each batch's accepted HSPs ("dedup") is timed apart
+from the step (--no-dedup skips it).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -45,6 +48,19 @@ def algorithmic_bytes(n_seeds: int, n_anchors: int, ref_len: int, qry_len: int) 
     reads, the prefix, the bucket start), 13 per anchor (4-byte position read,
     8-byte anchor write, 1-byte flag write), and both sequences once."""
     return 16 * n_seeds + 13 * n_anchors + ref_len + qry_len
+
+
+def workload_desc(args) -> str:
+    d = WORKLOAD_DESC.get(args.workload, args.workload)
+    return d if args.scale == 1.0 else "%s, scaled by %g (sizes and counts)" % (d, args.scale)
+
+
+def measured_sm_max_mhz() -> float:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("sm_max_mhz", 2070.0))
+    return 2070.0
 
 
 def measured_peaks():
@@ -139,7 +155,7 @@ def reference_arm(args):
         return 0
     from seed_hits_ungapped_gb300 import synth
     import oracle
-    w = synth.make(args.workload)
+    w = synth.make(args.workload, args.scale)
     idx, pos = oracle.build_index(w.ref)
     buckets = oracle.seed_buckets(w.query)
     P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
@@ -164,7 +180,7 @@ def reference_arm(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
-            "data": "synthetic", "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload)},
+            "data": "synthetic", "config": {"workload": workload_desc(args)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": "per step: expansion + gate + compaction + materialization of %d "
                                        "consecutive seeds of the %s query (single-threaded C oracle)"
@@ -183,6 +199,9 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dedup", action="store_true")
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="size factor of the workload (profiling on smaller cases; 1 = the workload as named)")
     ap.add_argument("--gate", default="fused", choices=["fused", "bucketed"],
                     help="fused expansion + gate (default), or expansion then the reference-bucketed gate (D.5)")
     args = ap.parse_args()
@@ -208,7 +227,7 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    w = synth.make(args.workload)
+    w = synth.make(args.workload, args.scale)
     lib = hspz.load_library()
     eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
     stream = torch.cuda.current_stream()
@@ -289,15 +308,64 @@ def main():
     alg_bytes_per_launch = step_bytes * args.steps / n_launch
     achieved = step_bytes * args.steps / (sum(gate_ms) / 1e3) / 1e9
     peak, peak_kind = measured_peaks()
+    # ncu counters of the same kernel version (null once the CUDA sources change)
     traffic = None
+    prof = {}
     tp = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tp):
         try:
             tr = json.load(open(tp))
-            if tr.get("workload") == args.workload and tr.get("kernel_rev") == kernel_rev():
+            if tr.get("workload") == args.workload and args.scale == 1.0 and tr.get("kernel_rev") == kernel_rev():
+                prof = tr
                 traffic = tr.get("bytes_per_launch")
         except Exception:
-            traffic = None
+            prof = {}
+    # the second roofline: issued instructions against the SMs' issue rate
+    # (4 schedulers x 32 lanes per SM per cycle at the maximum SM clock)
+    issue = None
+    if prof.get("warp_inst_per_launch"):
+        wi = float(prof["warp_inst_per_launch"])
+        t_launch = sum(gate_ms) / n_launch / 1e3
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        sm_mhz = measured_sm_max_mhz()
+        peak_issue = sms * 128 * sm_mhz * 1e6 / 1e12
+        achieved_issue = wi * 32 / t_launch / 1e12
+        issue = {"bound": "issue", "achieved": achieved_issue, "peak": peak_issue,
+                 "unit": "T lane-instructions/s (warp instructions x 32)", "frac": achieved_issue / peak_issue,
+                 "warp_inst_per_anchor": wi / (n_anchors * args.steps / n_launch),
+                 "active_lane_frac": (float(prof["thread_inst_per_launch"]) / (wi * 32)
+                                      if prof.get("thread_inst_per_launch") else None),
+                 "peak_basis": "%d SMs x 128 x %.0f MHz" % (sms, sm_mhz),
+                 "source": prof.get("source")}
+
+    # duplicate removal over each batch's accepted HSPs, timed apart from the step
+    dedup = None
+    if not args.no_dedup:
+        n_acc_all = n_fin_all = 0
+        dd_ms = []
+        for it in range(args.warmup + 3):
+            tot = 0.0
+            n_acc_all = n_fin_all = 0
+            for dq in d_queries:
+                r = eng.run(dq, max_hits=w.max_hits, dedup=True)  # collects the batch's accepted records
+                batch = eng._bufs.get("batch_records")
+                if not r.n_accepted:
+                    continue
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                ids, k = eng.dedup(batch, r.n_accepted)
+                e1.record(stream)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+                n_acc_all += r.n_accepted
+                n_fin_all += k
+            if it >= args.warmup:
+                dd_ms.append(tot)
+        med = statistics.median(dd_ms)
+        dedup = {"records": n_acc_all, "final": n_fin_all, "ms_per_step": med,
+                 "records_per_s": n_acc_all / (med / 1e3) if med > 0 else None,
+                 "timing": "CUDA events around hspz_dedup (it reads the kept count back to host)"}
 
     # end to end through the public API with host buffers
     e2e = None
@@ -340,7 +408,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload), "anchors_per_step": n_anchors,
+        "config": {"workload": workload_desc(args), "anchors_per_step": n_anchors,
                    "seeds_per_step": n_seeds, "survivors": n_surv_step, "accepted": n_acc_step,
                    "chunks": n_chunks_step, "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
@@ -351,6 +419,8 @@ def main():
                                 "expansion + bucket sort + k_gate_rounds (reference-bucketed gate)"),
                      "kernel_ms_per_launch": sum(gate_ms) / n_launch,
                      "algorithmic_bytes_per_launch": alg_bytes_per_launch},
+        "issue_roofline": issue,
+        "dedup": dedup,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": int(launches),
@@ -362,11 +432,12 @@ def main():
 
 
 def kernel_rev() -> str:
-    """Content hash of the CUDA sources (ties stored ncu traffic to a kernel version)."""
+    """Content hash of the sources that define the fused expansion + gate
+    kernel (ties stored ncu counters to a kernel version)."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "seed_hits_ungapped_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in ("hspz_gate.cu", "hspz_internal.cuh"):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 

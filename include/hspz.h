@@ -269,6 +269,32 @@ int hspz_materialize(const hspz_index *index, const hspz_plan *plan, const hspz_
                      const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
 
 /* ------------------------------------------------------------------------ *
+ * Record gather: d_out[k] = d_records[d_idx[k]] for k < n (16-byte records;
+ * both arrays 16-byte aligned; every d_idx[k] must index d_records).  Collects
+ * a chunk's accepted records (d_idx = the accepted survivor indices written
+ * by hspz_compact over the done flags) into a batch-wide array for
+ * hspz_dedup, and the kept records after it.  Asynchronous on `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_gather_records(const hspz_segment_pair *d_records, const uint32_t *d_idx, uint64_t n,
+                        hspz_segment_pair *d_out, void *stream);
+
+/* ------------------------------------------------------------------------ *
+ * Duplicate removal over the accepted HSPs of one query batch ("D. Score
+ * gate": the accepted raw HSPs become the final HSPs after dedup; "C. Hit
+ * discovery", C.5: the raw anchor order sets the dedup scope).  The pages do
+ * not state the criterion.  Reading taken here: record i of d_records (the
+ * batch's accepted records in raw order, n of them, 16-byte aligned) is
+ * dropped when a record j < i has the same four fields.  d_keep_ids receives
+ * the indices of the kept records in increasing order and *n_kept their
+ * count; if the count exceeds cap nothing is written to d_keep_ids and
+ * HSPZ_E_CAPACITY is returned with *n_kept set.  n <= 2^31 (else
+ * HSPZ_E_INVAL).  Uses stream-ordered scratch of about 8n + n bytes from the
+ * device's default memory pool.  Synchronizes `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_ids, uint64_t cap,
+               uint64_t *n_kept, void *stream);
+
+/* ------------------------------------------------------------------------ *
  * Host-only chunk walk over a host prefix array, exactly the walk
  * hspz_find_hits runs (use_block_sums != 0: lower bound located through the
  * 256-count block sums, then inside one block; 0: over the whole array).

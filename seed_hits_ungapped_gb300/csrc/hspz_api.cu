@@ -538,6 +538,51 @@ int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t 
     return total > cap ? HSPZ_E_CAPACITY : HSPZ_OK;
 }
 
+int hspz_gather_records(const hspz_segment_pair *d_records, const uint32_t *d_idx, uint64_t n,
+                        hspz_segment_pair *d_out, void *stream) {
+    if (n && (!d_records || !d_idx || !d_out)) return HSPZ_E_INVAL;
+    if ((reinterpret_cast<uintptr_t>(d_records) | reinterpret_cast<uintptr_t>(d_out)) & 15u) return HSPZ_E_INVAL;
+    cudaError_t e = launch_gather_records(d_records, d_idx, n, d_out, (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_gather_records");
+}
+
+int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_ids, uint64_t cap, uint64_t *n_kept,
+               void *stream) {
+    if (!n_kept || (n && !d_records) || n > (1ull << 31)) return HSPZ_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(d_records) & 15u) return HSPZ_E_INVAL;
+    if (cap && !d_keep_ids) return HSPZ_E_INVAL;
+    *n_kept = 0;
+    if (!n) return HSPZ_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    // scratch: table | keep flags (n bytes, word-padded) | compaction scratch | total, error count
+    // (the keep flags and the compaction scratch start on 16-byte boundaries)
+    const uint64_t slots = dedup_table_slots(n), keep_words = (n + 15) / 16 * 4, cw = compact_scratch_words(n);
+    const uint64_t words = slots + keep_words + cw + 6;
+    uint32_t *scratch = nullptr;
+    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_dedup scratch");
+    uint32_t *d_tab = scratch;
+    uint8_t *d_keep = reinterpret_cast<uint8_t *>(scratch + slots);
+    uint32_t *d_cs = scratch + slots + keep_words;
+    uint64_t *d_tail = reinterpret_cast<uint64_t *>(scratch + ((slots + keep_words + cw + 1) & ~1ull));
+    uint64_t tail[2] = {0, 0};  // total kept, probe failures
+    e = cudaMemsetAsync(d_tail, 0, 16, st);
+    if (e == cudaSuccess)
+        e = launch_dedup(d_records, n, d_tab, slots, d_keep, reinterpret_cast<unsigned long long *>(d_tail + 1), st);
+    if (e == cudaSuccess) e = launch_compact(d_keep, n, 0, d_keep_ids, cap, d_cs, d_tail, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(tail, d_tail, 16, cudaMemcpyDeviceToHost, st);
+    cudaError_t ef = cudaFreeAsync(scratch, st);
+    if (e == cudaSuccess) e = ef;
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_dedup");
+    if (tail[1]) {
+        set_error("hspz_dedup: hash probe sequence exhausted");
+        return HSPZ_E_UNSUPPORTED;
+    }
+    *n_kept = tail[0];
+    return tail[0] > cap ? HSPZ_E_CAPACITY : HSPZ_OK;
+}
+
 int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n_anchors,
                      uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids, const hspz_score_params *params,
                      hspz_segment_pair *d_out, uint8_t *d_done, void *stream) {

@@ -101,6 +101,13 @@ uint64_t compact_scratch_words(uint64_t n);
 cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
                            uint32_t *d_scratch, uint64_t *d_total, cudaStream_t st, const uint64_t *d_n = nullptr);
 
+// duplicate removal (two passes over a table of dedup_table_slots(n) uint32, keep flags out)
+uint64_t dedup_table_slots(uint64_t n);
+cudaError_t launch_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_tab, uint64_t slots,
+                         uint8_t *d_keep, unsigned long long *d_err, cudaStream_t st);
+cudaError_t launch_gather_records(const hspz_segment_pair *d_records, const uint32_t *d_idx, uint64_t n,
+                                  hspz_segment_pair *d_out, cudaStream_t st);
+
 }  // namespace hspz
 
 struct hspz_index {

@@ -37,6 +37,12 @@ class BatchResult:
     chunks: np.ndarray
     per_chunk: List[ChunkResult]
     prefix: Optional[np.ndarray] = None
+    # with dedup: the final HSPs, i.e. the batch's accepted records in raw
+    # order with exact duplicates dropped (first kept)
+    n_final: int = 0
+    d_final: Optional[object] = None                # (n_final, 4) int32 device tensor
+    final_records: Optional[np.ndarray] = None      # host copy, with keep or fetch
+    final_idx: Optional[np.ndarray] = None          # kept indices into the accepted list, with keep
 
     @property
     def n_survivors(self):
@@ -92,6 +98,30 @@ class HspEngine:
             ids = self.buffer(name, e.needed, torch.int32)
             return ids, hspz.hspz_compact(flags, n, id_base, ids, stream=self.stream)
 
+    def _append_rows(self, name: str, k: int, n: int, cols: int):
+        """Room for n more rows after the first k of an int32 buffer, keeping them."""
+        torch = self.torch
+        have = self._bufs.get(name)
+        if have is None or have.shape[0] < k + n:
+            rows = max(k + n, int(1.25 * have.shape[0]) if have is not None else 0, 1024)
+            new = torch.empty((rows, cols), dtype=torch.int32, device="cuda")
+            if have is not None and k:
+                new[:k].copy_(have[:k])
+            self._bufs[name] = new
+        return self._bufs[name]
+
+    def dedup(self, d_records, n: int):
+        """hspz_dedup into the engine's id buffer: (kept ids tensor, count)."""
+        torch = self.torch
+        ids = self.buffer("final_ids", max(1, n // 2), torch.int32)
+        try:
+            return ids, hspz.hspz_dedup(d_records, n, ids, stream=self.stream)
+        except hspz.HspzError as e:
+            if e.status != hspz.HSPZ_E_CAPACITY:
+                raise
+            ids = self.buffer("final_ids", e.needed, torch.int32)
+            return ids, hspz.hspz_dedup(d_records, n, ids, stream=self.stream)
+
     def plan(self, d_query, max_hits: int = 0, walk_full: bool = False):
         return hspz.hspz_find_hits(self.index, d_query, max_hits, walk_full, stream=self.stream)
 
@@ -117,12 +147,16 @@ class HspEngine:
                 cap = int(e.needed * 1.1) + 1024
 
     def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False,
-            fetch: bool = False) -> BatchResult:
+            fetch: bool = False, dedup: bool = False) -> BatchResult:
         """The whole path over one query batch.  keep=True copies every
         intermediate of every chunk to host; fetch=True copies only the
-        results (records, done flags, accepted ids) of every chunk."""
+        results (records, done flags, accepted ids) of every chunk.
+        dedup=True also collects the accepted records of all chunks in raw
+        order and drops exact duplicates (hspz_gather_records, hspz_dedup)."""
+        torch = self.torch
         plan = self.plan(d_query, max_hits, walk_full)
         out = []
+        n_acc_total = 0
         for c in range(plan.n_chunks):
             hb = int(plan.chunks[c, 2])
             n, n_surv, n_acc, _ = self.process_chunk(plan, c)
@@ -140,9 +174,24 @@ class HspEngine:
                 r.records = rec[:n_surv].cpu().numpy()
                 r.done = done[:n_surv].cpu().numpy()
                 r.accepted = _np_u32(acc[:n_acc])
+            if dedup and n_acc:
+                batch = self._append_rows("batch_records", n_acc_total, n_acc, 4)
+                hspz.hspz_gather_records(rec, acc, n_acc, batch[n_acc_total:], stream=self.stream)
+                n_acc_total += n_acc
             out.append(r)
         res = BatchResult(plan.n_seeds, plan.total_hits, plan.chunks.copy(), out)
         if keep:
             res.prefix = _np_u32(plan.prefix())
+        if dedup:
+            batch = self._append_rows("batch_records", n_acc_total, 0, 4)
+            ids, n_final = self.dedup(batch, n_acc_total)
+            final = self.buffer("final_records", max(1, n_final), torch.int32, 4)
+            hspz.hspz_gather_records(batch, ids, n_final, final, stream=self.stream)
+            res.n_final = n_final
+            res.d_final = final[:n_final]
+            if keep or fetch:
+                res.final_records = final[:n_final].cpu().numpy()
+            if keep:
+                res.final_idx = _np_u32(ids[:n_final]).copy()
         plan.close()
         return res

@@ -35,6 +35,7 @@ EXPORTS = [
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
     "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed", "hspz_process_chunk",
+    "hspz_gather_records", "hspz_dedup",
 ]
 
 
@@ -89,6 +90,8 @@ def load_library():
         "hspz_compact": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_materialize": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
         "hspz_chunk_walk_host": (ctypes.c_int, [VP, U64, U64, ctypes.c_int, P(hspz_chunk), U32, P(U32)]),
+        "hspz_gather_records": (ctypes.c_int, [VP, VP, U64, VP, VP]),
+        "hspz_dedup": (ctypes.c_int, [VP, U64, VP, U64, P(U64), VP]),
         "hspz_kernel_launches": (U64, []),
         "hspz_compact_noalloc": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_compact_noalloc_max_flags": (U64, []),
@@ -375,6 +378,34 @@ def hspz_materialize(index: Index, plan: Plan, d_anchors, id_base: int, d_ids, n
                                          ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
                                          _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
     _check(rc, "hspz_materialize")
+
+
+def hspz_gather_records(d_records, d_idx, n: int, d_out, stream=None):
+    """d_out[k] = d_records[d_idx[k]] for k < n ((m, 4) int32 record tensors)."""
+    import torch
+    if d_idx.numel() < n or d_out.numel() < 4 * n:
+        raise ValueError("buffers shorter than n")
+    rc = load_library().hspz_gather_records(_dptr(d_records, torch.int32, "d_records"), _dptr(d_idx, torch.int32, "d_idx"),
+                                            int(n), _dptr(d_out, torch.int32, "d_out"), _stream(stream))
+    _check(rc, "hspz_gather_records")
+
+
+def hspz_dedup(d_records, n: int, d_keep_ids, stream=None) -> int:
+    """Indices of the first of every group of equal records among the first n,
+    in increasing order, into d_keep_ids; returns their count."""
+    import torch
+    if d_records.numel() < 4 * n:
+        raise ValueError("records shorter than n")
+    out = ctypes.c_uint64(0)
+    rc = load_library().hspz_dedup(_dptr(d_records, torch.int32, "d_records"), int(n),
+                                   _dptr(d_keep_ids, torch.int32, "d_keep_ids"), d_keep_ids.numel(),
+                                   ctypes.byref(out), _stream(stream))
+    if rc == HSPZ_E_CAPACITY:
+        err = HspzError(rc, "hspz_dedup", "needs %d ids" % out.value)
+        err.needed = out.value
+        raise err
+    _check(rc, "hspz_dedup")
+    return out.value
 
 
 def hspz_chunk_walk_host(prefix: np.ndarray, max_hits: int, use_block_sums: bool = True) -> np.ndarray:
