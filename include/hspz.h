@@ -106,6 +106,13 @@ int hspz_abi_version(void);
 /* Number of CUDA kernels this library has launched in this process (all
  * devices, all threads); lets a caller count the launches of a region. */
 uint64_t hspz_kernel_launches(void);
+/* Device memory the library allocates per call (plans, scratch, index-build
+ * temporaries) comes from one stream-ordered memory pool per device owned by
+ * the library; memory freed back to it stays cached for the next call instead
+ * of being returned to the driver.  This returns every pool's cached memory
+ * that no allocation holds (cudaMemPoolTrimTo).  Memory still held by live
+ * plans or by frees not yet reached on their streams stays in the pools. */
+int hspz_release_cached_memory(void);
 
 /* ------------------------------------------------------------------------ *
  * Keep threshold ("D. Score gate", D.2 invariant): the least integer total t
@@ -143,7 +150,7 @@ int hspz_index_tables(const hspz_index *index, const uint32_t **d_idx, const uin
  * total <= max_hits or max_hits == 0, else the lower-bound walk over the seed
  * prefixes that keeps the straddling seed whole.  flags: 0 or HSPZ_WALK_FULL.
  * The plan keeps pointers into `index`.  Its device buffers come from the
- * device's stream-ordered memory pool on `stream`, and hspz_plan_free returns
+ * library's stream-ordered memory pool on `stream`, and hspz_plan_free returns
  * them in that stream's order, so free a plan only with its work queued on
  * that stream (or finished).  Synchronizes `stream`.
  * ------------------------------------------------------------------------ */
@@ -226,8 +233,8 @@ int hspz_score_gate_bucketed(const hspz_index *index, const hspz_plan *plan, con
  * Stable compaction ("D. Score gate", D.4): d_ids receives id_base + i for
  * every i < n with d_flags[i] != 0, in increasing order; *n_out receives the
  * count.  If the count exceeds cap nothing is written and HSPZ_E_CAPACITY is
- * returned with *n_out set.  Uses stream-ordered scratch from the device's
- * default memory pool.  Synchronizes `stream`.
+ * returned with *n_out set.  Uses stream-ordered scratch from the library's
+ * memory pool.  Synchronizes `stream`.
  * ------------------------------------------------------------------------ */
 int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
                  uint64_t *n_out, void *stream);
@@ -289,7 +296,7 @@ int hspz_gather_records(const hspz_segment_pair *d_records, const uint32_t *d_id
  * count; if the count exceeds cap nothing is written to d_keep_ids and
  * HSPZ_E_CAPACITY is returned with *n_kept set.  n <= 2^31 (else
  * HSPZ_E_INVAL).  Uses stream-ordered scratch of about 8n + n bytes from the
- * device's default memory pool.  Synchronizes `stream`.
+ * library's memory pool.  Synchronizes `stream`.
  * ------------------------------------------------------------------------ */
 int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_ids, uint64_t cap,
                uint64_t *n_kept, void *stream);

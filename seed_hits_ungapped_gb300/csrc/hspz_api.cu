@@ -25,6 +25,53 @@ constexpr int64_t kMaxX = 1ll << 30;
 constexpr int64_t kMaxAbsScore = 1ll << 16;
 }  // namespace
 
+// ------------------------------------------------------------------ memory pool
+// Stream-ordered allocations of the library (plans, per-call scratch, index
+// build temporaries) come from one pool per device that keeps freed memory
+// cached (release threshold = unlimited), so a plan or scratch buffer of the
+// same size as before is handed out again without mapping new memory.
+// hspz_release_cached_memory trims the pools back.
+namespace {
+constexpr int kMaxPoolDevices = 64;
+std::mutex g_pool_mutex;
+cudaMemPool_t g_pools[kMaxPoolDevices] = {};
+
+cudaError_t device_pool(cudaMemPool_t *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxPoolDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (!g_pools[dev]) {
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t pool;
+        e = cudaMemPoolCreate(&pool, &props);
+        if (e != cudaSuccess) return e;
+        uint64_t keep = UINT64_MAX;
+        e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+        if (e != cudaSuccess) {
+            cudaMemPoolDestroy(pool);
+            return e;
+        }
+        g_pools[dev] = pool;
+    }
+    *out = g_pools[dev];
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t st) {
+    cudaMemPool_t pool;
+    cudaError_t e = device_pool(&pool);
+    if (e != cudaSuccess) return e;
+    return cudaMallocFromPoolAsync(p, bytes ? bytes : 1, pool, st);
+}
+
+cudaError_t pool_free(void *p, cudaStream_t st) { return p ? cudaFreeAsync(p, st) : cudaSuccess; }
+
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
@@ -178,6 +225,16 @@ const char *hspz_last_error(void) { return g_last_error.c_str(); }
 
 int hspz_abi_version(void) { return HSPZ_ABI_VERSION; }
 
+int hspz_release_cached_memory(void) {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    for (int d = 0; d < kMaxPoolDevices; d++) {
+        if (!g_pools[d]) continue;
+        cudaError_t e = cudaMemPoolTrimTo(g_pools[d], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "hspz_release_cached_memory");
+    }
+    return HSPZ_OK;
+}
+
 uint64_t hspz_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int hspz_keep_threshold(int32_t K, int32_t *T_out) {
@@ -206,13 +263,13 @@ int hspz_build_index(const uint8_t *d_ref, uint64_t ref_len, const char *seed_pa
     if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref, ix->ref_words * 4);
     if (e == cudaSuccess) e = cudaMalloc((void **)&ix->d_ref_rev, ix->ref_words * 4);
     unsigned long long *d_ncount = nullptr, ncount = 0;
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&d_ncount, 8, st);
+    if (e == cudaSuccess) e = pool_alloc(&d_ncount, 8, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(d_ncount, 0, 8, st);
     if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 0, ix->d_ref, ix->ref_words, st, d_ncount);
     if (e == cudaSuccess) e = launch_pack(d_ref, ref_len, 1, 1, ix->d_ref_rev, ix->ref_words, st);
     if (e == cudaSuccess) e = build_index_tables(d_ref, ref_len, sh, ix->d_idx, &ix->d_pos, &ix->n_pos, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&ncount, d_ncount, 8, cudaMemcpyDeviceToHost, st);
-    if (d_ncount) cudaFreeAsync(d_ncount, st);
+    if (d_ncount) pool_free(d_ncount, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     ix->has_n = ncount != 0;
     if (e != cudaSuccess) {
@@ -254,7 +311,7 @@ void hspz_plan_free(hspz_plan *p) {
     // queued on the plan's stream so far has finished
     for (void *q : {(void *)p->d_P, (void *)p->d_lo, (void *)p->d_cnt, (void *)p->d_blk, (void *)p->d_qry,
                     (void *)p->d_qry_rev, (void *)p->d_tiles})
-        if (q) cudaFreeAsync(q, p->stream);
+        if (q) pool_free(q, p->stream);
     delete p;
 }
 
@@ -276,12 +333,12 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     cudaError_t e = cudaSuccess;
     const uint64_t sa = S ? S : 1;
     p->stream = st;
-    e = cudaMallocAsync((void **)&p->d_P, sa * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_lo, sa * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_cnt, sa * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_blk, (3 * nb + 2) * 8, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry, p->qry_words * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&p->d_qry_rev, p->qry_words * 4, st);
+    e = pool_alloc(&p->d_P, sa * 4, st);
+    if (e == cudaSuccess) e = pool_alloc(&p->d_lo, sa * 4, st);
+    if (e == cudaSuccess) e = pool_alloc(&p->d_cnt, sa * 4, st);
+    if (e == cudaSuccess) e = pool_alloc(&p->d_blk, (3 * nb + 2) * 8, st);
+    if (e == cudaSuccess) e = pool_alloc(&p->d_qry, p->qry_words * 4, st);
+    if (e == cudaSuccess) e = pool_alloc(&p->d_qry_rev, p->qry_words * 4, st);
     // the total and the query's N count sit side by side after the block sums
     uint64_t *bsum = p->d_blk, *bexcl = p->d_blk + nb, *bincl = p->d_blk + 2 * nb, *dtot = p->d_blk + 3 * nb;
     if (e == cudaSuccess) e = cudaMemsetAsync(dtot, 0, 16, st);
@@ -345,7 +402,7 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     p->max_chunk_hits = 0;
     for (const auto &c : p->chunks)
         p->max_chunk_hits = std::max<uint64_t>(p->max_chunk_hits, (uint64_t)c.hit_end - c.hit_begin);
-    e = cudaMallocAsync((void **)&p->d_tiles, expand_gate_tile_words(p->max_chunk_hits) * 4, st);
+    e = pool_alloc(&p->d_tiles, expand_gate_tile_words(p->max_chunk_hits) * 4, st);
     if (e != cudaSuccess) {
         rc = cuda_fail(e, "hspz_find_hits tile scratch");
         hspz_plan_free(p);
@@ -435,7 +492,7 @@ int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_para
     uint64_t totals[2] = {0, 0};
     SeqView r{p->index->d_ref, p->index->ref_len, p->index->d_ref_rev, p->index->has_n},
         q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
-    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    cudaError_t e = pool_alloc(&scratch, words * 4, st);
     // the two counts sit after the compaction scratch, 8-byte aligned
     uint64_t *tot = reinterpret_cast<uint64_t *>(scratch + ((words - 6) & ~1ull));
     if (e == cudaSuccess && gate_ms) {
@@ -457,7 +514,7 @@ int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_para
         e = cudaMemsetAsync(tot + 1, 0, 8, st);
     }
     if (e == cudaSuccess) e = cudaMemcpyAsync(totals, tot, 16, cudaMemcpyDeviceToHost, st);
-    cudaError_t ef = scratch ? cudaFreeAsync(scratch, st) : cudaSuccess;
+    cudaError_t ef = scratch ? pool_free(scratch, st) : cudaSuccess;
     if (e == cudaSuccess) e = ef;
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e == cudaSuccess && gate_ms) e = cudaEventElapsedTime(gate_ms, ev0, ev1);
@@ -504,14 +561,14 @@ int hspz_score_gate_bucketed(const hspz_index *ix, const hspz_plan *p, const hsp
     const uint32_t span = (uint32_t)((Lr + n_buckets - 1) / n_buckets);
     hspz_anchor *sorted = nullptr;
     uint32_t *raw = nullptr, *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync((void **)&sorted, n * sizeof(hspz_anchor), st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&raw, n * 4, st);
-    if (e == cudaSuccess) e = cudaMallocAsync((void **)&scratch, bucket_scratch_words(n, n_buckets) * 4, st);
+    cudaError_t e = pool_alloc(&sorted, n * sizeof(hspz_anchor), st);
+    if (e == cudaSuccess) e = pool_alloc(&raw, n * 4, st);
+    if (e == cudaSuccess) e = pool_alloc(&scratch, bucket_scratch_words(n, n_buckets) * 4, st);
     if (e == cudaSuccess) e = launch_bucket_sort(d_anchors, n, span, n_buckets, sorted, raw, scratch, st);
     SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     if (e == cudaSuccess) e = launch_gate(sorted, raw, n, r, q, sa, d_flags, st);
     for (void *ptr : {(void *)sorted, (void *)raw, (void *)scratch})
-        if (ptr) cudaFreeAsync(ptr, st);
+        if (ptr) pool_free(ptr, st);
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate_bucketed");
 }
 
@@ -524,13 +581,13 @@ int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t 
     if (!n) return HSPZ_OK;
     uint32_t *scratch = nullptr;
     const uint64_t words = compact_scratch_words(n) + 2;
-    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    cudaError_t e = pool_alloc(&scratch, words * 4, st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_compact scratch");
     uint64_t *d_total = reinterpret_cast<uint64_t *>(scratch + ((words - 2) & ~1ull));
     uint64_t total = 0;
     e = launch_compact(d_flags, n, id_base, d_ids, cap, scratch, d_total, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&total, d_total, 8, cudaMemcpyDeviceToHost, st);
-    cudaError_t ef = cudaFreeAsync(scratch, st);
+    cudaError_t ef = pool_free(scratch, st);
     if (e == cudaSuccess) e = ef;
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_compact");
@@ -559,7 +616,7 @@ int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_
     const uint64_t slots = dedup_table_slots(n), keep_words = (n + 15) / 16 * 4, cw = compact_scratch_words(n);
     const uint64_t words = slots + keep_words + cw + 6;
     uint32_t *scratch = nullptr;
-    cudaError_t e = cudaMallocAsync((void **)&scratch, words * 4, st);
+    cudaError_t e = pool_alloc(&scratch, words * 4, st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_dedup scratch");
     uint32_t *d_tab = scratch;
     uint8_t *d_keep = reinterpret_cast<uint8_t *>(scratch + slots);
@@ -571,7 +628,7 @@ int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_
         e = launch_dedup(d_records, n, d_tab, slots, d_keep, reinterpret_cast<unsigned long long *>(d_tail + 1), st);
     if (e == cudaSuccess) e = launch_compact(d_keep, n, 0, d_keep_ids, cap, d_cs, d_tail, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(tail, d_tail, 16, cudaMemcpyDeviceToHost, st);
-    cudaError_t ef = cudaFreeAsync(scratch, st);
+    cudaError_t ef = pool_free(scratch, st);
     if (e == cudaSuccess) e = ef;
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_dedup");

@@ -364,10 +364,10 @@ cudaError_t build_index_tables(const uint8_t *d_ref, uint64_t ref_len, const See
         e = (x);                      \
         if (e != cudaSuccess) goto out; \
     } while (0)
-    TRY(cudaMallocAsync((void **)&flags, n_win, st));
-    TRY(cudaMallocAsync((void **)&starts, n_win * 4, st));
-    TRY(cudaMallocAsync((void **)&scratch, compact_scratch_words(n_win) * 4, st));
-    TRY(cudaMallocAsync((void **)&d_n, 8, st));
+    TRY(pool_alloc(&flags, n_win, st));
+    TRY(pool_alloc(&starts, n_win * 4, st));
+    TRY(pool_alloc(&scratch, compact_scratch_words(n_win) * 4, st));
+    TRY(pool_alloc(&d_n, 8, st));
     k_window_flags<<<grid_for(n_win, 256), 256, 0, st>>>(d_ref, n_win, sh, flags); count_launch();
     TRY(cudaGetLastError());
     TRY(launch_compact(flags, n_win, 0, starts, n_win, scratch, d_n, st));
@@ -376,11 +376,11 @@ cudaError_t build_index_tables(const uint8_t *d_ref, uint64_t ref_len, const See
     if (n) {
         const uint64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
         (void)n_tiles_max;
-        TRY(cudaMallocAsync((void **)&k0, n * 4, st));
-        TRY(cudaMallocAsync((void **)&v0, n * 4, st));
-        TRY(cudaMallocAsync((void **)&k1, n * 4, st));
-        TRY(cudaMallocAsync((void **)&v1, n * 4, st));
-        TRY(cudaMallocAsync((void **)&hist, n_tiles * 256 * 4, st));
+        TRY(pool_alloc(&k0, n * 4, st));
+        TRY(pool_alloc(&v0, n * 4, st));
+        TRY(pool_alloc(&k1, n * 4, st));
+        TRY(pool_alloc(&v1, n * 4, st));
+        TRY(pool_alloc(&hist, n_tiles * 256 * 4, st));
         k_window_keys<<<grid_for(n, 256), 256, 0, st>>>(d_ref, starts, n, sh, k0, v0); count_launch();
         TRY(cudaGetLastError());
         const int smem = kRadixThreads * 256 * 2;
@@ -407,7 +407,7 @@ out:
 #undef TRY
     for (void *p : {(void *)flags, (void *)starts, (void *)scratch, (void *)k0, (void *)v0, (void *)k1, (void *)v1,
                     (void *)hist, (void *)d_n})
-        if (p) cudaFreeAsync(p, st);
+        if (p) pool_free(p, st);
     cudaError_t e2 = cudaStreamSynchronize(st);
     return e != cudaSuccess ? e : e2;
 }

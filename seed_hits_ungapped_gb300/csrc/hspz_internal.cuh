@@ -52,6 +52,14 @@ int parse_pattern(const char *pat, SeedShape *sh);
 int make_score_args(const hspz_score_params *p, ScoreArgs *out);
 uint64_t packed_words(uint64_t len);
 
+// stream-ordered allocation from the library's caching pool of the current device
+cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t st);
+template <typename T>
+cudaError_t pool_alloc(T **p, size_t bytes, cudaStream_t st) {
+    return pool_alloc(reinterpret_cast<void **>(p), bytes, st);
+}
+cudaError_t pool_free(void *p, cudaStream_t st);
+
 // kernel launch accounting (every launch site calls count_launch(k) for k launches)
 void count_launch(uint64_t k = 1);
 

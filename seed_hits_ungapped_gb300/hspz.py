@@ -35,7 +35,7 @@ EXPORTS = [
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
     "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed", "hspz_process_chunk",
-    "hspz_gather_records", "hspz_dedup",
+    "hspz_gather_records", "hspz_dedup", "hspz_release_cached_memory",
 ]
 
 
@@ -74,6 +74,7 @@ def load_library():
         "hspz_strerror": (ctypes.c_char_p, [ctypes.c_int]),
         "hspz_last_error": (ctypes.c_char_p, []),
         "hspz_abi_version": (ctypes.c_int, []),
+        "hspz_release_cached_memory": (ctypes.c_int, []),
         "hspz_keep_threshold": (ctypes.c_int, [I32, P(I32)]),
         "hspz_build_index": (ctypes.c_int, [VP, U64, ctypes.c_char_p, P(VP), VP]),
         "hspz_index_free": (None, [VP]),
@@ -378,6 +379,11 @@ def hspz_materialize(index: Index, plan: Plan, d_anchors, id_base: int, d_ids, n
                                          ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
                                          _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
     _check(rc, "hspz_materialize")
+
+
+def hspz_release_cached_memory():
+    """Return the library pools' cached device memory to the driver."""
+    _check(load_library().hspz_release_cached_memory(), "hspz_release_cached_memory")
 
 
 def hspz_gather_records(d_records, d_idx, n: int, d_out, stream=None):

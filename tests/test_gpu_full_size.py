@@ -104,6 +104,8 @@ def test_full_size_sampled(torch_cuda, name):
     w = synth.make(name)
     checked = sampled_parity(torch_cuda, w)
     assert checked > 100_000_000
+    from seed_hits_ungapped_gb300 import hspz
+    hspz.hspz_release_cached_memory()
     torch_cuda.cuda.empty_cache()
 
 

@@ -120,6 +120,18 @@ def test_chunk_walk_modes_agree(torch_cuda):
     assert_same_as_oracle(a, orc)
 
 
+def test_release_cached_memory_between_runs(torch_cuda):
+    """Trimming the library's memory pools between two runs changes nothing."""
+    from seed_hits_ungapped_gb300 import hspz
+    w = synth.make("chunking", scale=0.02)
+    eng = _engine(torch_cuda, w.ref, w.matrix, w.xdrop, w.K)
+    a = eng.run(_dev(torch_cuda, w.query), max_hits=w.max_hits, keep=True)
+    hspz.hspz_release_cached_memory()
+    b = eng.run(_dev(torch_cuda, w.query), max_hits=w.max_hits, keep=True)
+    for x, y in zip(a.per_chunk, b.per_chunk):
+        assert np.array_equal(x.flags, y.flags) and np.array_equal(x.records, y.records)
+
+
 def test_run_fetch_returns_every_chunk(torch_cuda):
     """fetch=True (the results-only copy the end-to-end timing uses) hands
     back each chunk's own records, done flags and accepted ids."""
