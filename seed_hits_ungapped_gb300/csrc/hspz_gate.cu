@@ -374,6 +374,46 @@ __device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint
     return false;
 }
 
+// walk_step_exact without branches, for the steps every lane of a round runs
+// together: a lane whose side is over (or that has no walk) keeps its state,
+// and only its loads are skipped.
+template <bool HAS_N>
+__device__ __forceinline__ void walk_step_exact_sel(WalkState &w, bool &stepping, uint32_t tlo, uint32_t thi,
+                                                    const int *__restrict__ tab25, int X, int need) {
+    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
+    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
+    int Sv[8];
+    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
+    int m = w.M, d = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        d |= Sv[k] + X - m;
+        m = max(m, Sv[k]);
+    }
+    const bool over = ((d | (need - 1 - m)) < 0) | (w.rem <= 8);
+    const bool adv = stepping && !over;
+    w.M = stepping ? m : w.M;
+    stepping = adv;
+    w.rem = adv ? w.rem - 8u : w.rem;
+    w.S = adv ? Sv[7] : w.S;
+    w.r0 = adv ? w.r1 : w.r0;
+    w.q0 = adv ? w.q1 : w.q0;
+    w.pr += adv ? 1 : 0;
+    w.pq += adv ? 1 : 0;
+    if (adv) {
+        w.r1 = __ldg(w.pr + 1);
+        w.q1 = __ldg(w.pq + 1);
+    }
+}
+
+// Steps of each side that a round runs without votes before its vote loop.
+// A round lasts the longest walk of its 32 lanes (for random anchors ~8 steps
+// on the left, ~6 on the right), so these steps are rarely extra, and a
+// branch-free step costs fewer instructions than a step of the vote loop and
+// lets consecutive steps overlap.  Measured on workload_a: (7, 5) beat
+// shorter and longer leads.
+constexpr int kLeadLeft = 7, kLeadRight = 5;
+
 // One synchronous round of 32 anchors, one per lane (`walk0` false for an
 // empty slot): all lanes start their left side together, step until every
 // lane's side is over, then do the right side the same way.  The right
@@ -412,6 +452,14 @@ __device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, 
         }
         bool stepping = walk;
         if (EXACT) {
+            if (!walk) w = WalkState{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+            if (side == 0) {
+#pragma unroll
+                for (int i = 0; i < kLeadLeft; i++) walk_step_exact_sel<HAS_N>(w, stepping, tlo, thi, tab, X, need);
+            } else {
+#pragma unroll
+                for (int i = 0; i < kLeadRight; i++) walk_step_exact_sel<HAS_N>(w, stepping, tlo, thi, tab, X, need);
+            }
             while (__any_sync(kFullMask, stepping)) {
                 if (stepping && walk_step_exact<HAS_N>(w, tlo, thi, tab, X, need)) stepping = false;
             }
