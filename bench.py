@@ -437,7 +437,7 @@ def kernel_rev() -> str:
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "seed_hits_ungapped_gb300", "csrc")
-    for f in ("hspz_gate.cu", "hspz_internal.cuh"):
+    for f in ("hspz_gate.cu", "hspz_walk.cuh", "hspz_internal.cuh"):
         h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 

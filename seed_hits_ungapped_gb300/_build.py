@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libhspz.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
-SOURCES = ["hspz_api.cu", "hspz_hits.cu", "hspz_gate.cu", "hspz_compact.cu", "hspz_noalloc.cu", "hspz_bucket.cu", "hspz_dedup.cu"]
+SOURCES = ["hspz_api.cu", "hspz_hits.cu", "hspz_gate.cu", "hspz_compact.cu", "hspz_noalloc.cu", "hspz_bucket.cu", "hspz_dedup.cu", "hspz_materialize.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC] + ARCH
 

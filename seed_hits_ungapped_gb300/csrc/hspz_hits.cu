@@ -95,11 +95,50 @@ __global__ void __launch_bounds__(kCountBlock) k_count(const uint8_t *__restrict
     }
 }
 
-// Single-CTA scan of n values (8 per thread per round): exclusive and
-// inclusive prefixes in OutT and the total.  Used for block sums.
+// Scan of n values in three launches (reduce, scan of the tile sums,
+// downsweep), every access coalesced: a tile is 1024 values, read as 4 rows of
+// 256 (thread t takes value 256k + t of row k).  `in` may be `excl` (scan in
+// place): every value is read before it is written.
+constexpr int kScanThreads = 256;
+constexpr int kScanRows = 4;
+constexpr int kScanTile = kScanThreads * kScanRows;
+
+template <typename T>
+__device__ __forceinline__ T block_excl_scan(T v, T *wtot, T *row_total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const T x = warp_incl_scan<T>(v, lane);
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    T pre = x - v, tot = 0;
+#pragma unroll
+    for (int w = 0; w < kScanThreads / 32; w++) {
+        pre += w < warp ? wtot[w] : (T)0;
+        tot += wtot[w];
+    }
+    __syncthreads();
+    *row_total = tot;
+    return pre;
+}
+
 template <typename InT, typename OutT>
-__global__ void __launch_bounds__(1024) k_scan(const InT *__restrict__ in, uint64_t n, OutT *__restrict__ excl,
-                                               OutT *__restrict__ incl, OutT *__restrict__ total) {
+__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(const InT *in, uint64_t n, OutT *__restrict__ part) {
+    __shared__ OutT wtot[kScanThreads / 32];
+    const uint64_t base = blockIdx.x * (uint64_t)kScanTile + threadIdx.x;
+    OutT v = 0;
+#pragma unroll
+    for (int k = 0; k < kScanRows; k++) {
+        const uint64_t i = base + (uint64_t)k * kScanThreads;
+        v += i < n ? (OutT)in[i] : (OutT)0;
+    }
+    OutT tot;
+    block_excl_scan<OutT>(v, wtot, &tot);
+    if (threadIdx.x == 0) part[blockIdx.x] = tot;
+}
+
+// Single-CTA scan of the tile sums (8 per thread per round), in place: the
+// exclusive prefix of every tile, and the total.
+template <typename OutT>
+__global__ void __launch_bounds__(1024) k_scan_parts(OutT *part, uint64_t n, OutT *__restrict__ total) {
     constexpr int kItems = 8;
     __shared__ OutT wtot[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -110,25 +149,20 @@ __global__ void __launch_bounds__(1024) k_scan(const InT *__restrict__ in, uint6
         const uint64_t i0 = base + (uint64_t)threadIdx.x * kItems;
 #pragma unroll
         for (int k = 0; k < kItems; k++) {
-            v[k] = (i0 + k < n) ? (OutT)in[i0 + k] : (OutT)0;
+            v[k] = (i0 + k < n) ? part[i0 + k] : (OutT)0;
             run += v[k];
         }
         OutT x = warp_incl_scan<OutT>(run, lane);
         if (lane == 31) wtot[warp] = x;
         __syncthreads();
-        if (warp == 0) {
-            OutT t = wtot[lane];
-            t = warp_incl_scan<OutT>(t, lane);
-            wtot[lane] = t;
-        }
+        if (warp == 0) wtot[lane] = warp_incl_scan<OutT>(wtot[lane], lane);
         __syncthreads();
         OutT pre = carry + (warp ? wtot[warp - 1] : (OutT)0) + (x - run);
 #pragma unroll
         for (int k = 0; k < kItems; k++) {
             if (i0 + k < n) {
-                if (excl) excl[i0 + k] = pre;
+                part[i0 + k] = pre;
                 pre += v[k];
-                if (incl) incl[i0 + k] = pre;
             }
         }
         carry += wtot[31];
@@ -137,19 +171,82 @@ __global__ void __launch_bounds__(1024) k_scan(const InT *__restrict__ in, uint6
     if (threadIdx.x == 0 && total) *total = carry;
 }
 
-// Local inclusive scan of 256 counts plus the block's exclusive offset (C.2).
+template <typename InT, typename OutT>
+__global__ void __launch_bounds__(kScanThreads) k_scan_down(const InT *in, uint64_t n,
+                                                            const OutT *__restrict__ part_excl, OutT *excl,
+                                                            OutT *__restrict__ incl) {
+    __shared__ OutT wtot[kScanThreads / 32];
+    OutT off = part_excl[blockIdx.x];
+    const uint64_t base = blockIdx.x * (uint64_t)kScanTile + threadIdx.x;
+#pragma unroll
+    for (int k = 0; k < kScanRows; k++) {
+        const uint64_t i = base + (uint64_t)k * kScanThreads;
+        const OutT v = i < n ? (OutT)in[i] : (OutT)0;
+        OutT row;
+        const OutT e = off + block_excl_scan<OutT>(v, wtot, &row);
+        if (i < n) {
+            if (excl) excl[i] = e;
+            if (incl) incl[i] = e + v;
+        }
+        off += row;
+    }
+}
+
+template <typename InT, typename OutT>
+cudaError_t launch_scan(const InT *d_in, uint64_t n, OutT *d_excl, OutT *d_incl, OutT *d_total, cudaStream_t st) {
+    if (!n) return d_total ? cudaMemsetAsync(d_total, 0, sizeof(OutT), st) : cudaSuccess;
+    const uint64_t tiles = (n + kScanTile - 1) / kScanTile;
+    OutT *part = nullptr;
+    cudaError_t e = pool_alloc(&part, tiles * sizeof(OutT), st);
+    if (e != cudaSuccess) return e;
+    k_scan_reduce<InT, OutT><<<(unsigned)tiles, kScanThreads, 0, st>>>(d_in, n, part); count_launch();
+    k_scan_parts<OutT><<<1, 1024, 0, st>>>(part, tiles, d_total); count_launch();
+    k_scan_down<InT, OutT><<<(unsigned)tiles, kScanThreads, 0, st>>>(d_in, n, part, d_excl, d_incl); count_launch();
+    e = cudaGetLastError();
+    cudaError_t ef = pool_free(part, st);
+    return e != cudaSuccess ? e : ef;
+}
+
+// Inclusive prefix (C.2): 1024 counts per CTA, 4 per thread, plus the
+// exclusive offset of the CTA's first 256-count block.
+constexpr int kPrefixPerThread = 4;
+constexpr int kPrefixTile = kCountBlock * kPrefixPerThread;
+
 __global__ void __launch_bounds__(kCountBlock) k_prefix(const uint32_t *__restrict__ cnt, uint64_t n,
                                                         const uint64_t *__restrict__ bexcl, uint32_t *__restrict__ P) {
     __shared__ uint64_t wtot[kCountBlock / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint64_t s = blockIdx.x * (uint64_t)kCountBlock + threadIdx.x;
-    uint64_t v = s < n ? cnt[s] : 0;
-    uint64_t x = warp_incl_scan<uint64_t>(v, lane);
+    const uint64_t s = blockIdx.x * (uint64_t)kPrefixTile + (uint64_t)threadIdx.x * kPrefixPerThread;
+    uint32_t v[kPrefixPerThread];
+    if (s + kPrefixPerThread <= n) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(cnt + s);
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2] = q.z;
+        v[3] = q.w;
+    } else {
+#pragma unroll
+        for (int k = 0; k < kPrefixPerThread; k++) v[k] = s + k < n ? cnt[s + k] : 0u;
+    }
+    const uint64_t run = (uint64_t)v[0] + v[1] + v[2] + v[3];
+    const uint64_t x = warp_incl_scan<uint64_t>(run, lane);
     if (lane == 31) wtot[warp] = x;
     __syncthreads();
-    uint64_t pre = bexcl[blockIdx.x];
+    uint64_t pre = bexcl[(uint64_t)blockIdx.x * (kPrefixTile / kCountBlock)] + (x - run);
     for (int w = 0; w < warp; w++) pre += wtot[w];
-    if (s < n) P[s] = (uint32_t)(pre + x);
+    uint32_t o[kPrefixPerThread];
+#pragma unroll
+    for (int k = 0; k < kPrefixPerThread; k++) {
+        pre += v[k];
+        o[k] = (uint32_t)pre;
+    }
+    if (s + kPrefixPerThread <= n) {
+        *reinterpret_cast<uint4 *>(P + s) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < kPrefixPerThread; k++)
+            if (s + k < n) P[s + k] = o[k];
+    }
 }
 
 // C.5, thread-per-seed mapping: occurrence j goes to slot P[s] - 1 - hit_begin - j.
@@ -308,20 +405,19 @@ cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedSha
 
 cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, uint64_t *d_incl, uint64_t *d_total,
                             cudaStream_t st) {
-    k_scan<uint64_t, uint64_t><<<1, 1024, 0, st>>>(d_in, n, d_excl, d_incl, d_total); count_launch();
-    return cudaGetLastError();
+    return launch_scan<uint64_t, uint64_t>(d_in, n, d_excl, d_incl, d_total, st);
 }
 
 cudaError_t launch_scan_u32(const uint32_t *d_in, uint64_t n, uint32_t *d_excl, cudaStream_t st) {
-    k_scan<uint32_t, uint32_t><<<1, 1024, 0, st>>>(d_in, n, d_excl, nullptr, nullptr); count_launch();
-    return cudaGetLastError();
+    return launch_scan<uint32_t, uint32_t>(d_in, n, d_excl, (uint32_t *)nullptr, (uint32_t *)nullptr, st);
 }
 
 cudaError_t launch_prefix(const uint32_t *d_cnt, uint64_t n_seeds, const uint64_t *d_block_excl, uint32_t *d_P,
                           cudaStream_t st) {
-    uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
-    if (!nb) return cudaSuccess;
-    k_prefix<<<(unsigned)nb, kCountBlock, 0, st>>>(d_cnt, n_seeds, d_block_excl, d_P); count_launch();
+    // cnt and P are 16-byte aligned (whole allocations); tiles of 1024 counts
+    const uint64_t nt = (n_seeds + kPrefixTile - 1) / kPrefixTile;
+    if (!nt) return cudaSuccess;
+    k_prefix<<<(unsigned)nt, kCountBlock, 0, st>>>(d_cnt, n_seeds, d_block_excl, d_P); count_launch();
     return cudaGetLastError();
 }
 
@@ -388,8 +484,7 @@ cudaError_t build_index_tables(const uint8_t *d_ref, uint64_t ref_len, const See
         for (int shift = 0; shift < 2 * sh.weight; shift += 8) {
             k_radix_hist<<<(unsigned)n_tiles, kRadixThreads, 0, st>>>(k0, n, shift, hist, n_tiles); count_launch();
             TRY(cudaGetLastError());
-            k_scan<uint32_t, uint32_t><<<1, 1024, 0, st>>>(hist, n_tiles * 256, hist, nullptr, nullptr); count_launch();
-            TRY(cudaGetLastError());
+            TRY(launch_scan_u32(hist, n_tiles * 256, hist, st));
             k_radix_scatter<<<(unsigned)n_tiles, kRadixThreads, smem, st>>>(k0, v0, n, shift, hist, n_tiles, k1, v1); count_launch();
             TRY(cudaGetLastError());
             uint32_t *t = k0; k0 = k1; k1 = t;
