@@ -188,80 +188,78 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
 // shorter and longer leads.
 constexpr int kLeadLeft = 7, kLeadRight = 5;
 
-// One synchronous round of 32 anchors, one per lane (`walk0` false for an
-// empty slot): all lanes start their left side together, step until every
-// lane's side is over, then do the right side the same way.  The right
-// side's first words are loaded with the left side's.  EXACT selects
-// walk_step_exact; otherwise flagged steps are settled by walk_resolve,
-// together, after every lane has flagged.  Returns the keep decision.
-template <bool HAS_N, bool EXACT>
-__device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, const uint32_t *__restrict__ ref_rev,
-                                           const uint32_t *__restrict__ qry_rev, uint32_t tlo, uint32_t thi,
-                                           const int *__restrict__ tab, int X, int T) {
-    bool accepted = false;
-    int need = T;
-    uint32_t nr0 = 0, nr1 = 0, nq0 = 0, nq1 = 0;  // the right side's first words
-#pragma unroll 1
-    for (int side = 0; side < 2; side++) {
-        const bool walk = walk0 && !accepted;
-        WalkState w;
-        if (walk) {
-            walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, side);
-            if (side == 0) {  // the left side's first words, and the right side's, in one go
-                w.r0 = __ldg(w.pr);
-                w.r1 = __ldg(w.pr + 1);
-                w.q0 = __ldg(w.pq);
-                w.q1 = __ldg(w.pq + 1);
-                const uint32_t jr = a.x + (uint32_t)kPadBases, jq = a.y + (uint32_t)kPadBases;
-                nr0 = __ldg(sq.ref + (jr >> 3));
-                nr1 = __ldg(sq.ref + (jr >> 3) + 1);
-                nq0 = __ldg(sq.qry + (jq >> 3));
-                nq1 = __ldg(sq.qry + (jq >> 3) + 1);
-            } else {
-                w.r0 = nr0;
-                w.r1 = nr1;
-                w.q0 = nq0;
-                w.q1 = nq1;
-            }
+// One side of a synchronous round.  Lanes with `walk` start together and step
+// until every lane's side is over (BACK: the left side, read downwards from
+// the anchor on the forward copies).  EXACT selects walk_step_exact;
+// otherwise flagged steps are settled by walk_resolve, together, after every
+// lane has flagged.  Leaves the side maximum in w.M and returns whether it
+// reached `need`.
+template <bool HAS_N, bool EXACT, bool BACK>
+__device__ __forceinline__ bool gate_side(WalkState &w, bool walk, uint32_t tlo, uint32_t thi,
+                                          const int *__restrict__ tab, int X, int need) {
+    bool stepping = walk;
+    if (EXACT) {
+        constexpr int lead = BACK ? kLeadLeft : kLeadRight;
+#pragma unroll
+        for (int i = 0; i < lead; i++) walk_step_exact_sel<HAS_N, BACK>(w, stepping, tlo, thi, tab, X, need);
+        while (__any_sync(kFullMask, stepping)) {
+            if (stepping && walk_step_exact<HAS_N, BACK>(w, tlo, thi, tab, X, need)) stepping = false;
         }
-        bool stepping = walk;
-        if (EXACT) {
-            if (!walk) w = WalkState{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
-            if (side == 0) {
-#pragma unroll
-                for (int i = 0; i < kLeadLeft; i++) walk_step_exact_sel<HAS_N>(w, stepping, tlo, thi, tab, X, need);
+        return walk && w.M >= need;
+    }
+    bool ended = !walk, accepted = false;
+    int Sv[8], Mb = 0;
+    bool maybe_stop = false;
+    while (__any_sync(kFullMask, !ended)) {
+        while (__any_sync(kFullMask, stepping)) {
+            if (stepping && walk_step<HAS_N, BACK>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
+        }
+        if (!ended) {
+            bool acc = false;
+            if (walk_resolve<BACK>(w, Sv, Mb, maybe_stop, X, need, &acc)) {
+                ended = true;
+                accepted = acc;
             } else {
-#pragma unroll
-                for (int i = 0; i < kLeadRight; i++) walk_step_exact_sel<HAS_N>(w, stepping, tlo, thi, tab, X, need);
-            }
-            while (__any_sync(kFullMask, stepping)) {
-                if (stepping && walk_step_exact<HAS_N>(w, tlo, thi, tab, X, need)) stepping = false;
-            }
-            if (walk) {
-                accepted = w.M >= need;
-                need = T - w.M;
-            }
-        } else {
-            bool ended = !walk;
-            int Sv[8], Mb = 0;
-            bool maybe_stop = false;
-            while (__any_sync(kFullMask, !ended)) {
-                while (__any_sync(kFullMask, stepping)) {
-                    if (stepping && walk_step<HAS_N>(w, tlo, thi, tab, X, need, Sv, Mb, maybe_stop)) stepping = false;
-                }
-                if (!ended) {
-                    bool acc = false;
-                    if (walk_resolve(w, Sv, Mb, maybe_stop, X, need, &acc)) {
-                        ended = true;
-                        accepted = acc;
-                        need = T - w.M;
-                    } else {
-                        stepping = true;
-                    }
-                }
+                stepping = true;
             }
         }
     }
+    return accepted;
+}
+
+// One synchronous round of 32 anchors, one per lane (`walk0` false for an
+// empty slot): all lanes walk their left side, then their right side, both
+// on the forward packed copies.  The left side's first window ends at the
+// anchor, so its upper words are the right side's first word; only one more
+// word per sequence is loaded for the right side, with the left side's.
+// Returns the keep decision.
+template <bool HAS_N, bool EXACT>
+__device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, uint32_t tlo, uint32_t thi,
+                                           const int *__restrict__ tab, int X, int T) {
+    WalkState w{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t nr1 = 0, nq1 = 0;  // the right side's second words
+    if (walk0) {
+        walk_place_fwd(w, sq, a.x, a.y, 0);
+        w.r0 = __ldg(w.pr);
+        w.r1 = __ldg(w.pr + 1);
+        w.q0 = __ldg(w.pq);
+        w.q1 = __ldg(w.pq + 1);
+        nr1 = __ldg(w.pr + 2);
+        nq1 = __ldg(w.pq + 2);
+    }
+    // the right side's first words: the left side's upper words before it moves
+    const uint32_t nr0 = w.r1, nq0 = w.q1;
+    bool accepted = gate_side<HAS_N, EXACT, true>(w, walk0, tlo, thi, tab, X, T);
+    const int need = T - w.M;
+    const bool walk1 = walk0 && !accepted;
+    if (walk1) {
+        walk_place_fwd(w, sq, a.x, a.y, 1);
+        w.r0 = nr0;
+        w.r1 = nr1;
+        w.q0 = nq0;
+        w.q1 = nq1;
+    }
+    accepted |= gate_side<HAS_N, EXACT, false>(w, walk1, tlo, thi, tab, X, need);
     return accepted;
 }
 
@@ -296,8 +294,7 @@ template <bool HAS_N, bool EXACT>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
     k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
                     const uint32_t *__restrict__ pos, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
-                    uint32_t span, Seqs sq, const uint32_t *__restrict__ ref_rev,
-                    const uint32_t *__restrict__ qry_rev, const uint32_t *__restrict__ tiles, ScoreArgs sa,
+                    uint32_t span, Seqs sq, const uint32_t *__restrict__ tiles, ScoreArgs sa,
                     uint2 *__restrict__ out, uint8_t *__restrict__ flags) {
     __shared__ uint2 sA_all[kWTile];
     __shared__ uint32_t sP[kWSeeds];
@@ -355,7 +352,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
         const bool valid = ai < count;
         uint2 a = make_uint2(0, 0);
         if (valid) a = sA[ai];
-        const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, ref_rev, qry_rev, tlo, thi, tab, X, T);
+        const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, tlo, thi, tab, X, T);
         if (valid) flags[t0 + ai] = accepted ? 1 : 0;
     }
     // 3. anchors
@@ -369,8 +366,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
 // anchor i goes to flags[raw ? raw[i] : i].
 template <bool HAS_N, bool EXACT>
 __global__ void __launch_bounds__(kWWarps * 32, 5)
-    k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq,
-                  const uint32_t *__restrict__ ref_rev, const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
+    k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq, ScoreArgs sa,
                   uint8_t *__restrict__ flags) {
     __shared__ int tab[25];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -388,7 +384,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
             uint2 a = make_uint2(0, 0);
             if (valid) a = anchors[t0 + ai];
             const bool inside = valid && a.x < sq.Lr && a.y < sq.Lq;
-            const bool accepted = gate_round<HAS_N, EXACT>(a, inside, sq, ref_rev, qry_rev, tlo, thi, tab, X, T);
+            const bool accepted = gate_round<HAS_N, EXACT>(a, inside, sq, tlo, thi, tab, X, T);
             if (valid) flags[raw ? raw[t0 + ai] : t0 + ai] = accepted ? 1 : 0;
         }
     }
@@ -427,8 +423,8 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
         k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
         auto kern = sa.exact ? (ref.has_n || qry.has_n ? k_expand_gate_w<true, true> : k_expand_gate_w<false, true>)
                              : (ref.has_n || qry.has_n ? k_expand_gate_w<true, false> : k_expand_gate_w<false, false>);
-        kern<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), ref.rev,
-                                                         qry.rev, d_tiles, sa, out, d_flags); count_launch();
+        kern<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), d_tiles, sa,
+                                                         out, d_flags); count_launch();
     } else {
         k_expand_gate<true><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     }
@@ -443,8 +439,8 @@ cudaError_t launch_gate(const hspz_anchor *d_anchors, const uint32_t *d_raw, uin
         const unsigned g = (unsigned)(want < 152ull * 40 ? want : 152ull * 40);
         auto kern = sa.exact ? (ref.has_n || qry.has_n ? k_gate_rounds<true, true> : k_gate_rounds<false, true>)
                              : (ref.has_n || qry.has_n ? k_gate_rounds<true, false> : k_gate_rounds<false, false>);
-        kern<<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n, seqs(ref, qry), ref.rev,
-                                         qry.rev, sa, d_flags); count_launch();
+        kern<<<g, kWWarps * 32, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), d_raw, n, seqs(ref, qry), sa,
+                                         d_flags); count_launch();
     } else if (!d_raw) {
         k_gate<false><<<grid_cap(n, 256), 256, 0, st>>>(reinterpret_cast<const uint2 *>(d_anchors), n, seqs(ref, qry), sa,
                                                          d_flags); count_launch();

@@ -87,6 +87,21 @@ __device__ __forceinline__ uint32_t low_nibbles(uint32_t n) {
     return ~d;
 }
 
+// Mask of the high min(n, 8) nibbles: the bases of a step of a walk that
+// reads the packed words downwards (walk order = nibbles 7..0).
+__device__ __forceinline__ uint32_t high_nibbles(uint32_t n) {
+    const uint32_t s = 32u - min(n, 8u) * 4u;
+    uint32_t d;
+    asm("shl.b32 %0, %1, %2;" : "=r"(d) : "r"(0xFFFFFFFFu), "r"(s));  // shifts of 32 give 0
+    return d;
+}
+
+// The bases of the step at the front of a walk of `rem` bases left.
+template <bool BACK>
+__device__ __forceinline__ uint32_t step_keep(uint32_t rem) {
+    return BACK ? high_nibbles(rem) : low_nibbles(rem);
+}
+
 struct WalkState {
     const uint32_t *pr, *pq;
     uint32_t shr, shq, r0, r1, q0, q1, rem;
@@ -109,26 +124,57 @@ __device__ __forceinline__ void walk_place(WalkState &w, const Seqs &sq, const u
     w.M = 0;
 }
 
+// Where one side of anchor (ar, aq) starts on the forward packed copies.
+// The right side (side 1) reads upwards from the anchor base.  The left side
+// (side 0) scores ar-1, ar-2, ... : its step window is the 8 bases just below
+// the current position, read from the same words downwards (BACK walks), so
+// the left and right walks of an anchor share the cache lines around it.
+__device__ __forceinline__ void walk_place_fwd(WalkState &w, const Seqs &sq, uint32_t ar, uint32_t aq, int side) {
+    const uint32_t Lr = (uint32_t)sq.Lr, Lq = (uint32_t)sq.Lq;
+    w.rem = side ? min(Lr - ar, Lq - aq) : min(ar, aq);
+    // unsigned wrap of ar - 8 for ar < 8 is undone by the padding offset
+    const uint32_t jr = (side ? ar : ar - 8u) + (uint32_t)kPadBases;
+    const uint32_t jq = (side ? aq : aq - 8u) + (uint32_t)kPadBases;
+    w.pr = sq.ref + (jr >> 3);
+    w.pq = sq.qry + (jq >> 3);
+    w.shr = (jr & 7u) * 4u;
+    w.shq = (jq & 7u) * 4u;
+    w.S = 0;
+    w.M = 0;
+}
+
+// Moves a walk one step on: the window words slide up (or down for BACK) by
+// one word and the newly needed word of each sequence is loaded.
+template <bool BACK = false>
 __device__ __forceinline__ void walk_advance(WalkState &w, int S_next) {
     w.rem -= 8;
     w.S = S_next;
-    w.r0 = w.r1;
-    w.q0 = w.q1;
-    w.pr++;
-    w.pq++;
-    w.r1 = __ldg(w.pr + 1);
-    w.q1 = __ldg(w.pq + 1);
+    if (BACK) {
+        w.r1 = w.r0;
+        w.q1 = w.q0;
+        w.pr--;
+        w.pq--;
+        w.r0 = __ldg(w.pr);
+        w.q0 = __ldg(w.pq);
+    } else {
+        w.r0 = w.r1;
+        w.q0 = w.q1;
+        w.pr++;
+        w.pq++;
+        w.r1 = __ldg(w.pr + 1);
+        w.q1 = __ldg(w.pq + 1);
+    }
 }
 
 // The common 8-base step.  It advances the walk and returns false unless the
 // step may hold the stop, reaches `need` or ends at the edge; then it leaves
 // the walk untouched and returns true for walk_resolve.
-template <bool HAS_N>
+template <bool HAS_N, bool BACK = false>
 __device__ __forceinline__ bool walk_step(WalkState &w, uint32_t tlo, uint32_t thi, const int *__restrict__ tab25,
                                           int X, int need, int (&Sv)[8], int &Mb, bool &maybe_stop) {
     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
-    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
+    step_sums<!BACK, HAS_N>(R, Q, step_keep<BACK>(w.rem), tlo, thi, tab25, w.S, Sv);
     const int hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
     const int lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
     Mb = max(w.M, hi);
@@ -137,7 +183,7 @@ __device__ __forceinline__ bool walk_step(WalkState &w, uint32_t tlo, uint32_t t
     maybe_stop = gap < 0;
     if (!(((gap | (need - 1 - Mb)) < 0) | (w.rem <= 8))) {
         w.M = Mb;
-        walk_advance(w, Sv[7]);
+        walk_advance<BACK>(w, Sv[7]);
         return false;
     }
     return true;
@@ -145,6 +191,7 @@ __device__ __forceinline__ bool walk_step(WalkState &w, uint32_t tlo, uint32_t t
 
 // Settles a flagged step.  Returns true when the side is over, with *acc
 // telling whether its maximum reached `need`; else the walk has advanced.
+template <bool BACK = false>
 __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], int Mb, bool maybe_stop, int X,
                                              int need, bool *acc) {
     if (maybe_stop) {
@@ -168,7 +215,7 @@ __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], i
         *acc = false;
         return true;
     }
-    walk_advance(w, Sv[7]);
+    walk_advance<BACK>(w, Sv[7]);
     return false;
 }
 
@@ -180,13 +227,13 @@ __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], i
 // side maximum at the stop: the step never has to be replayed base by base.
 // Returns true when the side is over (stop, `need` reached or edge) with
 // w.M = the side maximum; otherwise the walk has advanced.
-template <bool HAS_N>
+template <bool HAS_N, bool BACK = false>
 __device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint32_t thi,
                                                 const int *__restrict__ tab25, int X, int need) {
     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
     int Sv[8];
-    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
+    step_sums<!BACK, HAS_N>(R, Q, step_keep<BACK>(w.rem), tlo, thi, tab25, w.S, Sv);
     // d collects the sign of S(k) + X - m(k-1) for every base k
     int m = w.M, d = 0;
 #pragma unroll
@@ -196,20 +243,20 @@ __device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint
     }
     w.M = m;
     if (((d | (need - 1 - m)) < 0) | (w.rem <= 8)) return true;
-    walk_advance(w, Sv[7]);
+    walk_advance<BACK>(w, Sv[7]);
     return false;
 }
 
 // walk_step_exact without branches, for the steps every lane of a round runs
 // together: a lane whose side is over (or that has no walk) keeps its state,
 // and only its loads are skipped.
-template <bool HAS_N>
+template <bool HAS_N, bool BACK = false>
 __device__ __forceinline__ void walk_step_exact_sel(WalkState &w, bool &stepping, uint32_t tlo, uint32_t thi,
                                                     const int *__restrict__ tab25, int X, int need) {
     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
     int Sv[8];
-    step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab25, w.S, Sv);
+    step_sums<!BACK, HAS_N>(R, Q, step_keep<BACK>(w.rem), tlo, thi, tab25, w.S, Sv);
     int m = w.M, d = 0;
 #pragma unroll
     for (int k = 0; k < 8; k++) {
@@ -222,13 +269,24 @@ __device__ __forceinline__ void walk_step_exact_sel(WalkState &w, bool &stepping
     stepping = adv;
     w.rem = adv ? w.rem - 8u : w.rem;
     w.S = adv ? Sv[7] : w.S;
-    w.r0 = adv ? w.r1 : w.r0;
-    w.q0 = adv ? w.q1 : w.q0;
-    w.pr += adv ? 1 : 0;
-    w.pq += adv ? 1 : 0;
-    if (adv) {
-        w.r1 = __ldg(w.pr + 1);
-        w.q1 = __ldg(w.pq + 1);
+    if (BACK) {
+        w.r1 = adv ? w.r0 : w.r1;
+        w.q1 = adv ? w.q0 : w.q1;
+        w.pr -= adv ? 1 : 0;
+        w.pq -= adv ? 1 : 0;
+        if (adv) {
+            w.r0 = __ldg(w.pr);
+            w.q0 = __ldg(w.pq);
+        }
+    } else {
+        w.r0 = adv ? w.r1 : w.r0;
+        w.q0 = adv ? w.q1 : w.q0;
+        w.pr += adv ? 1 : 0;
+        w.pq += adv ? 1 : 0;
+        if (adv) {
+            w.r1 = __ldg(w.pr + 1);
+            w.q1 = __ldg(w.pq + 1);
+        }
     }
 }
 

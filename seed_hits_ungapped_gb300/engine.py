@@ -73,6 +73,7 @@ class HspEngine:
         self.params = hspz.score_params(matrix, xdrop, K)
         self.T = hspz.hspz_keep_threshold(K)
         self._bufs = {}
+        self._host_bufs = {}
 
     def buffer(self, name: str, n: int, dtype, cols: int = 1):
         """A reusable device buffer with room for n rows (grown geometrically)."""
@@ -97,6 +98,28 @@ class HspEngine:
                 raise
             ids = self.buffer(name, e.needed, torch.int32)
             return ids, hspz.hspz_compact(flags, n, id_base, ids, stream=self.stream)
+
+    def _torch_stream(self):
+        torch = self.torch
+        if self.stream is None:
+            return torch.cuda.current_stream()
+        if isinstance(self.stream, int):
+            return torch.cuda.ExternalStream(self.stream)
+        return self.stream
+
+    def _host_rows(self, name: str, k: int, n: int, dtype, cols: int = 1):
+        """Room for n more rows after the first k of a pinned host buffer
+        (grown geometrically; the first k rows are kept)."""
+        torch = self.torch
+        have = self._host_bufs.get(name)
+        if have is None or have.shape[0] < k + n:
+            rows = max(k + n, int(1.5 * have.shape[0]) if have is not None else 0, 1024)
+            new = torch.empty((rows, cols) if cols > 1 else (rows,), dtype=dtype, pin_memory=True)
+            if have is not None and k:
+                self._torch_stream().synchronize()  # copies still landing in the old buffer
+                new[:k].copy_(have[:k])
+            self._host_bufs[name] = new
+        return self._host_bufs[name]
 
     def _append_rows(self, name: str, k: int, n: int, cols: int):
         """Room for n more rows after the first k of an int32 buffer, keeping them."""
@@ -149,14 +172,18 @@ class HspEngine:
     def run(self, d_query, max_hits: int = 0, walk_full: bool = False, keep: bool = False,
             fetch: bool = False, dedup: bool = False) -> BatchResult:
         """The whole path over one query batch.  keep=True copies every
-        intermediate of every chunk to host; fetch=True copies only the
-        results (records, done flags, accepted ids) of every chunk.
+        intermediate of every chunk to host (fresh arrays); fetch=True copies
+        only the results (records, done flags, accepted ids) of every chunk,
+        asynchronously into engine-owned pinned host buffers, and returns
+        numpy views of them that stay valid until the engine's next run.
         dedup=True also collects the accepted records of all chunks in raw
         order and drops exact duplicates (hspz_gather_records, hspz_dedup)."""
         torch = self.torch
         plan = self.plan(d_query, max_hits, walk_full)
         out = []
         n_acc_total = 0
+        off_s = off_a = 0  # rows of the pinned result buffers used so far
+        views = []
         for c in range(plan.n_chunks):
             hb = int(plan.chunks[c, 2])
             n, n_surv, n_acc, _ = self.process_chunk(plan, c)
@@ -171,14 +198,28 @@ class HspEngine:
                 r.done = done[:n_surv].cpu().numpy().copy()
                 r.accepted = _np_u32(acc[:n_acc]).copy()
             elif fetch:
-                r.records = rec[:n_surv].cpu().numpy()
-                r.done = done[:n_surv].cpu().numpy()
-                r.accepted = _np_u32(acc[:n_acc])
+                h_rec = self._host_rows("records", off_s, n_surv, torch.int32, 4)
+                h_done = self._host_rows("done", off_s, n_surv, torch.uint8)
+                h_acc = self._host_rows("accepted", off_a, n_acc, torch.int32)
+                with torch.cuda.stream(self._torch_stream()):
+                    h_rec[off_s:off_s + n_surv].copy_(rec[:n_surv], non_blocking=True)
+                    h_done[off_s:off_s + n_surv].copy_(done[:n_surv], non_blocking=True)
+                    h_acc[off_a:off_a + n_acc].copy_(acc[:n_acc], non_blocking=True)
+                views.append((r, off_s, n_surv, off_a, n_acc))
+                off_s += n_surv
+                off_a += n_acc
             if dedup and n_acc:
                 batch = self._append_rows("batch_records", n_acc_total, n_acc, 4)
                 hspz.hspz_gather_records(rec, acc, n_acc, batch[n_acc_total:], stream=self.stream)
                 n_acc_total += n_acc
             out.append(r)
+        if views:
+            self._torch_stream().synchronize()
+            h_rec, h_done, h_acc = (self._host_bufs[k] for k in ("records", "done", "accepted"))
+            for r, os_, ns_, oa, na in views:
+                r.records = h_rec[os_:os_ + ns_].numpy()
+                r.done = h_done[os_:os_ + ns_].numpy()
+                r.accepted = h_acc[oa:oa + na].numpy().view(np.uint32)
         res = BatchResult(plan.n_seeds, plan.total_hits, plan.chunks.copy(), out)
         if keep:
             res.prefix = _np_u32(plan.prefix())
