@@ -186,7 +186,13 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
 // branch-free step costs fewer instructions than a step of the vote loop and
 // lets consecutive steps overlap.  Measured on workload_a: (7, 5) beat
 // shorter and longer leads.
-constexpr int kLeadLeft = 7, kLeadRight = 5;
+#ifndef HSPZ_LEAD_LEFT
+#define HSPZ_LEAD_LEFT 7
+#endif
+#ifndef HSPZ_LEAD_RIGHT
+#define HSPZ_LEAD_RIGHT 5
+#endif
+constexpr int kLeadLeft = HSPZ_LEAD_LEFT, kLeadRight = HSPZ_LEAD_RIGHT;
 
 // One side of a synchronous round.  Lanes with `walk` start together and step
 // until every lane's side is over (BACK: the left side, read downwards from
@@ -197,17 +203,18 @@ constexpr int kLeadLeft = 7, kLeadRight = 5;
 template <bool HAS_N, bool EXACT, bool BACK>
 __device__ __forceinline__ bool gate_side(WalkState &w, bool walk, uint32_t tlo, uint32_t thi,
                                           const int *__restrict__ tab, int X, int need) {
-    bool stepping = walk;
     if (EXACT) {
         constexpr int lead = BACK ? kLeadLeft : kLeadRight;
+        if (!walk) w.rem = 0;
 #pragma unroll
-        for (int i = 0; i < lead; i++) walk_step_exact_sel<HAS_N, BACK>(w, stepping, tlo, thi, tab, X, need);
+        for (int i = 0; i < lead; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
+        bool stepping = w.rem != 0;
         while (__any_sync(kFullMask, stepping)) {
             if (stepping && walk_step_exact<HAS_N, BACK>(w, tlo, thi, tab, X, need)) stepping = false;
         }
         return walk && w.M >= need;
     }
-    bool ended = !walk, accepted = false;
+    bool stepping = walk, ended = !walk, accepted = false;
     int Sv[8], Mb = 0;
     bool maybe_stop = false;
     while (__any_sync(kFullMask, !ended)) {

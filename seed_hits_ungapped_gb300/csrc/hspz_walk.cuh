@@ -247,12 +247,16 @@ __device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint
     return false;
 }
 
-// walk_step_exact without branches, for the steps every lane of a round runs
-// together: a lane whose side is over (or that has no walk) keeps its state,
-// and only its loads are skipped.
-template <bool HAS_N, bool BACK = false>
-__device__ __forceinline__ void walk_step_exact_sel(WalkState &w, bool &stepping, uint32_t tlo, uint32_t thi,
-                                                    const int *__restrict__ tab25, int X, int need) {
+// walk_step_exact for the steps every lane of a round runs together, without
+// branches or selects.  A lane whose side is over has rem = 0: its keep mask
+// is empty, so its later steps score nothing and leave S and M as they are
+// (S <= M holds throughout).  The window words and pointers move every step;
+// only the loads are skipped once rem = 0, so fully unrolled steps address
+// their words with immediate offsets.  Returns nothing: rem = 0 afterwards
+// means the side is over with w.M its maximum.
+template <bool HAS_N, bool BACK>
+__device__ __forceinline__ void walk_step_lead(WalkState &w, uint32_t tlo, uint32_t thi,
+                                               const int *__restrict__ tab25, int X, int need) {
     const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
     int Sv[8];
@@ -264,26 +268,24 @@ __device__ __forceinline__ void walk_step_exact_sel(WalkState &w, bool &stepping
         m = max(m, Sv[k]);
     }
     const bool over = ((d | (need - 1 - m)) < 0) | (w.rem <= 8);
-    const bool adv = stepping && !over;
-    w.M = stepping ? m : w.M;
-    stepping = adv;
-    w.rem = adv ? w.rem - 8u : w.rem;
-    w.S = adv ? Sv[7] : w.S;
+    w.M = m;
+    w.S = Sv[7];
+    w.rem = over ? 0u : w.rem - 8u;
     if (BACK) {
-        w.r1 = adv ? w.r0 : w.r1;
-        w.q1 = adv ? w.q0 : w.q1;
-        w.pr -= adv ? 1 : 0;
-        w.pq -= adv ? 1 : 0;
-        if (adv) {
+        w.r1 = w.r0;
+        w.q1 = w.q0;
+        w.pr--;
+        w.pq--;
+        if (w.rem) {
             w.r0 = __ldg(w.pr);
             w.q0 = __ldg(w.pq);
         }
     } else {
-        w.r0 = adv ? w.r1 : w.r0;
-        w.q0 = adv ? w.q1 : w.q0;
-        w.pr += adv ? 1 : 0;
-        w.pq += adv ? 1 : 0;
-        if (adv) {
+        w.r0 = w.r1;
+        w.q0 = w.q1;
+        w.pr++;
+        w.pq++;
+        if (w.rem) {
             w.r1 = __ldg(w.pr + 1);
             w.q1 = __ldg(w.pq + 1);
         }
