@@ -3,9 +3,13 @@
 One step = the whole path over one synthetic query batch: hit discovery
 (count, prefix, chunk walk), fused expansion + score gate, stable compaction,
 materialization and the accepted compaction.  The metric is anchors per
-second; the dominant kernel (fused expansion + gate) is also reported against
-the HBM roofline ("roofline") and, from ncu instruction counts of the same
-kernel version, against the SMs' instruction issue rate ("issue_roofline").
+second.  The dominant kernel (fused expansion + gate) is bound by integer
+arithmetic: "roofline" reports it against the SMs' int32 rate, counting 4
+operations per base pair the gate decision scores (pairs per anchor measured
+by the oracle on the CPU sample).  It is also reported against the HBM copy
+rate ("hbm_roofline"; "roofline" itself when the CPU sample is skipped) and,
+from ncu instruction counts of the same kernel version, against the SMs'
+instruction issue rate ("issue_roofline").
 Duplicate removal over each batch's accepted HSPs ("dedup") is timed apart
 from the step (--no-dedup skips it).
 
@@ -132,6 +136,7 @@ def run_cpu_baseline(w, seconds: float = 12.0):
     P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
     T = oracle.keep_threshold(w.K)
     done_anchors, t_used, s_begin = 0, 0.0, 0
+    pairs = pair_anchors = 0
     step_seeds = 200_000
     while t_used < seconds and s_begin < P.size:
         s_end = min(P.size, s_begin + step_seeds)
@@ -142,10 +147,16 @@ def run_cpu_baseline(w, seconds: float = 12.0):
         oracle.gate(w.ref, w.query, a, w.matrix, w.xdrop, T)
         t_used += time.perf_counter() - t0
         done_anchors += len(a)
+        # untimed: the base pairs the gate decision needs, on every 16th anchor
+        sub = a[::16]
+        pair_anchors += len(sub)
+        pairs += oracle.gate_pairs(w.ref, w.query, sub, w.matrix, w.xdrop, T)
         s_begin = s_end
     return {"value": done_anchors / t_used, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "expansion + gate of the first %d seeds (%d anchors) of the %s query, single-threaded C"
-                      % (s_begin, done_anchors, w.name), "seconds": round(t_used, 3)}
+                      % (s_begin, done_anchors, w.name), "seconds": round(t_used, 3),
+            "gate_pairs_per_anchor": pairs / pair_anchors if pair_anchors else None,
+            "gate_pairs_sample": "oracle.gate_pairs over every 16th of those anchors (%d)" % pair_anchors}
 
 
 def reference_arm(args):
@@ -399,6 +410,30 @@ def main():
         dist.destroy_process_group()
     if rank != 0:
         return 0
+    kernel_name = ("k_expand_gate_w (fused expansion + score gate)" if args.gate == "fused" else
+                   "expansion + bucket sort + k_gate_rounds (reference-bucketed gate)")
+    hbm = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+           "traffic": traffic, "peak_kind": peak_kind, "kernel": kernel_name,
+           "kernel_ms_per_launch": sum(gate_ms) / n_launch,
+           "algorithmic_bytes_per_launch": alg_bytes_per_launch}
+    # the bound that holds: integer arithmetic.  Algorithmic work = the base
+    # pairs the gate decision scores (per anchor, from the oracle on the CPU
+    # sample) x 4 integer operations per pair (pair score, running sum,
+    # running maximum, drop test), against 128 int32 lanes per SM per cycle.
+    alu = None
+    if cpu and cpu.get("gate_pairs_per_anchor"):
+        sms = torch.cuda.get_device_properties(local).multi_processor_count
+        sm_mhz = measured_sm_max_mhz()
+        ppa = cpu["gate_pairs_per_anchor"]
+        pairs_launch = ppa * n_anchors * args.steps / n_launch
+        t_launch = sum(gate_ms) / n_launch / 1e3
+        a_ops = 4 * pairs_launch / t_launch / 1e12
+        p_ops = sms * 128 * sm_mhz * 1e6 / 1e12
+        alu = {"bound": "alu", "achieved": a_ops, "peak": p_ops, "unit": "T int32 ops/s", "frac": a_ops / p_ops,
+               "traffic": traffic, "peak_kind": "derived: %d SMs x 128 int32 lanes x %.0f MHz" % (sms, sm_mhz),
+               "kernel": kernel_name, "kernel_ms_per_launch": sum(gate_ms) / n_launch,
+               "ops_per_pair": 4, "gate_pairs_per_anchor": ppa, "gate_pairs_per_launch": pairs_launch,
+               "pairs_basis": cpu.get("gate_pairs_sample")}
     # survivor, accepted and chunk counts over every query batch of one step
     results = [eng.run(dq, max_hits=w.max_hits) for dq in d_queries]
     n_surv_step = sum(r.n_survivors for r in results)
@@ -413,12 +448,8 @@ def main():
                    "chunks": n_chunks_step, "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "expand_gate_anchors_per_s": n_anchors * args.steps / (sum(gate_ms) / 1e3),
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "peak_kind": peak_kind,
-                     "kernel": ("k_expand_gate_w (fused expansion + score gate)" if args.gate == "fused" else
-                                "expansion + bucket sort + k_gate_rounds (reference-bucketed gate)"),
-                     "kernel_ms_per_launch": sum(gate_ms) / n_launch,
-                     "algorithmic_bytes_per_launch": alg_bytes_per_launch},
+        "roofline": alu if alu else hbm,
+        "hbm_roofline": hbm if alu else None,
         "issue_roofline": issue,
         "dedup": dedup,
         "cpu_baseline": cpu,

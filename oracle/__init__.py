@@ -64,6 +64,8 @@ def _load():
             lib.orc_chunk_walk.argtypes = [P, U64, U64, P, U64, P]
             lib.orc_expand.argtypes = [P, P, P, P, P, ctypes.c_int, P]
             lib.orc_expand.restype = None
+            lib.orc_gate_pairs.argtypes = [P, U64, P, U64, P, U64, P, ctypes.c_int32, ctypes.c_int32]
+            lib.orc_gate_pairs.restype = U64
             lib.orc_anchor_at.argtypes = [P, P, P, P, U64, ctypes.c_int, U64, P]
             lib.orc_side_scores.argtypes = [P, U64, P, U64, P, U64, P, I32, P]
             lib.orc_side_scores.restype = None
@@ -218,6 +220,19 @@ def gate(ref, qry, anchors, matrix, xdrop: int, T: int) -> np.ndarray:
         _load().orc_gate(_p(ref), ref.size, _p(qry), qry.size, _p(a), a.shape[0],
                          _p(_mat(matrix)), int(xdrop), int(T), _p(flags))
     return flags
+
+
+def gate_pairs(ref, qry, anchors, matrix, xdrop: int, T: int) -> int:
+    """Base pairs the gate decision of these anchors scores (a measure of its
+    work): each left walk up to its stop, edge or maximum >= T, then, unless
+    it reached T, the right walk up to its stop, edge or left + right
+    maximum >= T."""
+    ref, qry = _u8(ref), _u8(qry)
+    a = np.ascontiguousarray(anchors, dtype=np.uint32).reshape(-1, 2)
+    if not a.shape[0]:
+        return 0
+    return int(_load().orc_gate_pairs(_p(ref), ref.size, _p(qry), qry.size, _p(a), a.shape[0],
+                                      _p(_mat(matrix)), int(xdrop), int(T)))
 
 
 def compact(flags, id_base: int = 0) -> np.ndarray:

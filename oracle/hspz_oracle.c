@@ -326,6 +326,58 @@ void orc_gate(const uint8_t *ref, uint64_t ref_len, const uint8_t *qry, uint64_t
 }
 
 /* ---------------------------------------------------------------------------
+ * Work of the gate decision, for measurement ("D.2", "D.3").  The flag is
+ * known as soon as the running maxima reach T (total >= T is monotone in
+ * either side's maximum), so the decision needs, per anchor: the left walk's
+ * base pairs up to its stop, its edge, or the first pair at which its
+ * maximum reaches T; then, unless that happened, the right walk's pairs up
+ * to its stop, its edge, or the first pair at which the left maximum plus
+ * its maximum reaches T.  Returns the sum of those pair counts over all
+ * anchors.  The walk is the one side_walk takes, counted as it goes.
+ * ------------------------------------------------------------------------- */
+static uint64_t side_walk_pairs(const uint8_t *ref, uint64_t ref_len, const uint8_t *qry, uint64_t qry_len,
+                                uint64_t ar, uint64_t aq, int right, const int32_t *m, int64_t X,
+                                int64_t need, int64_t *best)
+{
+    int64_t S = 0, M = 0;
+    uint64_t scored = 0;
+    for (uint64_t n = 1;; n++) {
+        uint64_t rp, qp;
+        if (right) {
+            rp = ar + n - 1;
+            qp = aq + n - 1;
+            if (rp >= ref_len || qp >= qry_len) break;
+        } else {
+            if (n > ar || n > aq) break;
+            rp = ar - n;
+            qp = aq - n;
+        }
+        S += m[5 * ref[rp] + qry[qp]];
+        scored = n;
+        if (M - S > X) break;
+        if (S > M) M = S;
+        if (M >= need) break;
+    }
+    *best = M;
+    return scored;
+}
+
+uint64_t orc_gate_pairs(const uint8_t *ref, uint64_t ref_len, const uint8_t *qry, uint64_t qry_len,
+                        const uint32_t *anchors, uint64_t n, const int32_t *m, int32_t X, int32_t T)
+{
+    uint64_t total = 0;
+    for (uint64_t i = 0; i < n; i++) {
+        int64_t ML, MR;
+        total += side_walk_pairs(ref, ref_len, qry, qry_len, anchors[2 * i], anchors[2 * i + 1], 0, m, X,
+                                 (int64_t)T, &ML);
+        if (ML < (int64_t)T)
+            total += side_walk_pairs(ref, ref_len, qry, qry_len, anchors[2 * i], anchors[2 * i + 1], 1, m, X,
+                                     (int64_t)T - ML, &MR);
+    }
+    return total;
+}
+
+/* ---------------------------------------------------------------------------
  * Stable compaction ("D.4"): the ids (id_base + i) of every set flag, in
  * increasing order.
  * ------------------------------------------------------------------------- */

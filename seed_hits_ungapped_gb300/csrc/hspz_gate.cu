@@ -182,10 +182,10 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
 
 // Steps of each side that a round runs without votes before its vote loop.
 // A round lasts the longest walk of its 32 lanes (for random anchors ~8 steps
-// on the left, ~6 on the right), so these steps are rarely extra, and a
-// branch-free step costs fewer instructions than a step of the vote loop and
-// lets consecutive steps overlap.  Measured on workload_a: (7, 5) beat
-// shorter and longer leads.
+// on the left, ~6 on the right), so these steps are rarely extra, and
+// unrolled steps without votes overlap and address their words with
+// immediate offsets.  Measured on workload_a: (7, 5) and (8, 5) beat shorter
+// and longer leads.
 #ifndef HSPZ_LEAD_LEFT
 #define HSPZ_LEAD_LEFT 7
 #endif
@@ -196,7 +196,7 @@ constexpr int kLeadLeft = HSPZ_LEAD_LEFT, kLeadRight = HSPZ_LEAD_RIGHT;
 
 // One side of a synchronous round.  Lanes with `walk` start together and step
 // until every lane's side is over (BACK: the left side, read downwards from
-// the anchor on the forward copies).  EXACT selects walk_step_exact;
+// the anchor on the forward copies).  EXACT selects walk_step_lead;
 // otherwise flagged steps are settled by walk_resolve, together, after every
 // lane has flagged.  Leaves the side maximum in w.M and returns whether it
 // reached `need`.
@@ -208,10 +208,8 @@ __device__ __forceinline__ bool gate_side(WalkState &w, bool walk, uint32_t tlo,
         if (!walk) w.rem = 0;
 #pragma unroll
         for (int i = 0; i < lead; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
-        bool stepping = w.rem != 0;
-        while (__any_sync(kFullMask, stepping)) {
-            if (stepping && walk_step_exact<HAS_N, BACK>(w, tlo, thi, tab, X, need)) stepping = false;
-        }
+        // the tail: the same steps under a warp vote, while any lane walks
+        while (__any_sync(kFullMask, w.rem != 0)) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
         return walk && w.M >= need;
     }
     bool stepping = walk, ended = !walk, accepted = false;

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
 }
 
 // k_materialize_lane for scoring where the 8-base stop test is exact
-// (X >= 7 x the largest pair score, see walk_step_exact).  Lanes step in
+// (X >= 7 x the largest pair score, see walk_step_lead).  Lanes step in
 // blocks of kMatBlock branch-free steps between checks: a lane whose side
 // ended keeps its state until the block is over, then, in a short divergent
 // settle, places the side's earliest maximum by scoring the step of its last

@@ -225,35 +225,13 @@ __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], i
 // before it.  After such a stop the remaining (at most 7) sums of the step
 // cannot climb back above m(k-1), so the step's final running maximum is the
 // side maximum at the stop: the step never has to be replayed base by base.
-// Returns true when the side is over (stop, `need` reached or edge) with
-// w.M = the side maximum; otherwise the walk has advanced.
-template <bool HAS_N, bool BACK = false>
-__device__ __forceinline__ bool walk_step_exact(WalkState &w, uint32_t tlo, uint32_t thi,
-                                                const int *__restrict__ tab25, int X, int need) {
-    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
-    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
-    int Sv[8];
-    step_sums<!BACK, HAS_N>(R, Q, step_keep<BACK>(w.rem), tlo, thi, tab25, w.S, Sv);
-    // d collects the sign of S(k) + X - m(k-1) for every base k
-    int m = w.M, d = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        d |= Sv[k] + X - m;
-        m = max(m, Sv[k]);
-    }
-    w.M = m;
-    if (((d | (need - 1 - m)) < 0) | (w.rem <= 8)) return true;
-    walk_advance<BACK>(w, Sv[7]);
-    return false;
-}
-
-// walk_step_exact for the steps every lane of a round runs together, without
-// branches or selects.  A lane whose side is over has rem = 0: its keep mask
-// is empty, so its later steps score nothing and leave S and M as they are
-// (S <= M holds throughout).  The window words and pointers move every step;
-// only the loads are skipped once rem = 0, so fully unrolled steps address
-// their words with immediate offsets.  Returns nothing: rem = 0 afterwards
-// means the side is over with w.M its maximum.
+// The step has no branches or selects, so every lane of a round runs it
+// together.  A lane whose side is over (stop, `need` reached or edge) gets
+// rem = 0: its keep mask is then empty, so its later steps score nothing and
+// leave S and M as they are (S <= M holds throughout).  The window words and
+// pointers move every step; only the loads are skipped once rem = 0, so fully
+// unrolled steps address their words with immediate offsets.  rem = 0
+// afterwards means the side is over with w.M its maximum.
 template <bool HAS_N, bool BACK>
 __device__ __forceinline__ void walk_step_lead(WalkState &w, uint32_t tlo, uint32_t thi,
                                                const int *__restrict__ tab25, int X, int need) {

@@ -406,3 +406,66 @@ def test_dedup_leaves_one_hsp_per_exact_copy():
     score = sum(DIAG_HOXD70[int(b)] for b in seg)
     assert res["final_rec"].tolist() == [[7_000, 50, 299, score]]
     assert res["final_idx"].tolist() == [0]
+
+
+def _side_pairs_np(m, ref, qry, ar, aq, right, X, need):
+    """Pairs a side walk scores, from prefix sums: the first n where the
+    drop below the running maximum passes X, the maximum reaches `need`, or
+    the sequence edge comes."""
+    if right:
+        r, q = ref[ar:], qry[aq:]
+        k = min(r.size, q.size)
+        sc = m[r[:k], q[:k]].astype(np.int64)
+    else:
+        k = min(ar, aq)
+        sc = m[ref[ar - k:ar][::-1], qry[aq - k:aq][::-1]].astype(np.int64)
+    if k == 0:
+        return 0, 0
+    S = np.cumsum(sc)
+    Mrun = np.maximum.accumulate(np.maximum(S, 0))
+    Mprev = np.concatenate([[0], Mrun[:-1]])
+    ends = [k]
+    drop = np.nonzero(Mprev - S > X)[0]
+    if drop.size:
+        ends.append(drop[0] + 1)
+    acc = np.nonzero(Mrun >= need)[0]
+    if acc.size:
+        ends.append(acc[0] + 1)
+    n = min(ends)
+    best = int(Mprev[n - 1]) if (drop.size and n == drop[0] + 1) else int(Mrun[n - 1])
+    return n, best
+
+
+@pytest.mark.parametrize("T", [3000, 400, 10 ** 9])
+def test_gate_pairs_matches_prefix_sum_form(T):
+    rng = np.random.default_rng(17 + T % 1000)
+    m = hoxd70()
+    m[0, 2] = -60  # asymmetric, so a transposed lookup changes the count
+    ref = rng.integers(0, 4, 3000).astype(np.uint8)
+    qry = rng.integers(0, 4, 2000).astype(np.uint8)
+    qry[500:1400] = ref[1000:1900]  # one long homology, so some walks reach T
+    qry[600:610] = 4
+    anchors = np.array([[1000 + i, 500 + i] for i in range(0, 900, 37)]
+                       + [[int(rng.integers(0, 3000)), int(rng.integers(0, 2000))] for _ in range(60)]
+                       + [[0, 5], [7, 0], [2999, 1999], [2999, 3]], dtype=np.uint32)
+    X = 300
+    want = 0
+    for ar, aq in anchors.astype(np.int64):
+        nl, ml = _side_pairs_np(m, ref, qry, ar, aq, False, X, T)
+        want += nl
+        if ml < T:
+            nr, _ = _side_pairs_np(m, ref, qry, ar, aq, True, X, T - ml)
+            want += nr
+    assert oracle.gate_pairs(ref, qry, anchors, m, X, T) == want
+
+
+def test_gate_pairs_closed_forms():
+    m = hoxd70()
+    s = np.full(500, 1, dtype=np.uint8)  # all C: every pair scores 100
+    # T out of reach: both walks run to the edges
+    assert oracle.gate_pairs(s, s, np.array([[200, 200]], np.uint32), m, 910, 10 ** 9) == 500
+    # left maximum reaches T = 1000 after 10 pairs: the right walk is not needed
+    assert oracle.gate_pairs(s, s, np.array([[200, 200]], np.uint32), m, 910, 1000) == 10
+    # left walk has 4 pairs (400), the right needs 6 more
+    assert oracle.gate_pairs(s, s, np.array([[4, 4]], np.uint32), m, 910, 1000) == 4 + 6
+    assert oracle.gate_pairs(s, s, np.zeros((0, 2), np.uint32), m, 910, 1000) == 0
