@@ -268,6 +268,9 @@ __device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, 
     return accepted;
 }
 
+#ifndef HSPZ_GATE_MIN_BLOCKS
+#define HSPZ_GATE_MIN_BLOCKS 5  // resident CTAs per SM the register budget allows
+#endif
 constexpr int kWWarps = 8;             // warps per CTA
 constexpr int kWUnit = 256;            // anchor slots per warp
 constexpr int kWTile = kWWarps * kWUnit;
@@ -296,7 +299,7 @@ __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32
 //      edge, settle together, then the same for the right side;
 //   3. the warp stores its anchors and flags with coalesced writes.
 template <bool HAS_N, bool EXACT>
-__global__ void __launch_bounds__(kWWarps * 32, 5)
+__global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
                     const uint32_t *__restrict__ pos, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
                     uint32_t span, Seqs sq, const uint32_t *__restrict__ tiles, ScoreArgs sa,
@@ -370,7 +373,7 @@ __global__ void __launch_bounds__(kWWarps * 32, 5)
 // anchors, 8 synchronous rounds of 32 as in k_expand_gate_w; the flag of
 // anchor i goes to flags[raw ? raw[i] : i].
 template <bool HAS_N, bool EXACT>
-__global__ void __launch_bounds__(kWWarps * 32, 5)
+__global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     k_gate_rounds(const uint2 *__restrict__ anchors, const uint32_t *__restrict__ raw, uint64_t n, Seqs sq, ScoreArgs sa,
                   uint8_t *__restrict__ flags) {
     __shared__ int tab[25];
