@@ -151,22 +151,67 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
     }
 }
 
+// Survivors on one diagonal share their walks.  Take survivor a and the next
+// survivor b on a's diagonal, d bases further on (the next entry of the id
+// list, when it lies on the same diagonal).  After its first d pairs a's right
+// walk scores exactly b's pairs, its running sum differs from b's by a
+// constant C (a's sum after d pairs), and as soon as a's walk stands at its
+// running maximum at a step count n0 >= d, b's running maximum at the same
+// base is b's running sum there too.  From then on a's maximum is C plus b's
+// maximum, a's drop test is b's drop test, and b cannot have stopped before
+// (its drops up to there were no larger than a's).  So a's side ends where
+// b's ends, with maximum C + M_b, first reached d + n_b pairs out if
+// C + M_b > S_a(n0), else at a's own earliest maximum so far.  Left walks
+// join the previous survivor's left walk the same way.  With CHAIN, a walk
+// stops at such a join (checked at step ends) and records (S_a(n0), its
+// earliest maximum, C); k_chain_resolve then settles the linked
+// survivors.  Every kChainSeg-th entry of the id list (a breaker) never
+// joins, so every segment of kChainSeg entries settles on its own; the
+// breakers' lanes come first, packed into warps of their own, since their
+// walks run the whole length of their homologies.
+#ifndef HSPZ_MATERIALIZE_CHAIN
+#define HSPZ_MATERIALIZE_CHAIN 1
+#endif
+constexpr bool kMaterializeChain = HSPZ_MATERIALIZE_CHAIN != 0;
+constexpr uint32_t kLinkR = 1, kLinkL = 2, kJoinR = 4, kJoinL = 8;
+constexpr uint64_t kChainSeg = 32;  // one warp settles a segment
+struct ChainSide {
+    long long M;  // the side maximum, or the running sum (and maximum) at the join
+    uint32_t n;   // pairs out to the earliest base of that maximum
+    int32_t C;    // joined: the running sum after the first d pairs
+};
+struct ChainInfo {
+    uint32_t flags;  // kLinkR / kLinkL: the next / previous entry is the neighbour on this diagonal; kJoinR, kJoinL
+    uint32_t dR;     // linked: bases along the diagonal to the next survivor
+};
+
+__device__ __forceinline__ uint2 survivor_anchor(const uint2 *__restrict__ anchors, uint64_t n_anchors,
+                                                 uint32_t id_base, const uint32_t *__restrict__ ids, uint64_t k) {
+    const uint32_t id = ids[k];
+    const uint64_t slot = (uint64_t)id - id_base;  // wraps above n_anchors when id < id_base
+    return (id >= id_base && slot < n_anchors) ? anchors[slot] : make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
+}
+
 // k_materialize_lane for scoring where the 8-base stop test is exact
 // (X >= 7 x the largest pair score, see walk_step_lead).  Lanes step in
 // blocks of kMatBlock branch-free steps between checks: a lane whose side
 // ended keeps its state until the block is over, then, in a short divergent
 // settle, places the side's earliest maximum by scoring the step of its last
 // rise again and starts its right side or finishes.  Same records as
-// k_materialize_lane.
+// k_materialize_lane.  With CHAIN, walks also end at joins (see ChainSide);
+// a survivor linked to a neighbour leaves its two sides in sR / sL and its
+// links in info for k_chain_resolve, every other survivor gets its record.
 constexpr int kMatBlock = 8;
 
-template <bool HAS_N>
+template <bool HAS_N, bool CHAIN>
 __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                             uint32_t id_base, const uint32_t *__restrict__ ids,
                                                             uint64_t n_ids, const uint64_t *__restrict__ d_n, Seqs sq,
                                                             const uint32_t *__restrict__ ref_rev,
                                                             const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
-                                                            uint4 *__restrict__ out, uint8_t *__restrict__ done) {
+                                                            uint4 *__restrict__ out, uint8_t *__restrict__ done,
+                                                            ChainSide *__restrict__ sR, ChainSide *__restrict__ sL,
+                                                            ChainInfo *__restrict__ info) {
     __shared__ int tab[25];
     if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
     __syncthreads();
@@ -177,15 +222,26 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
     // the grid-stride loop runs the same number of trips in every lane of a warp
     const uint64_t first = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
     const uint64_t trips = (n_ids + stride - 1) / stride;
+    const uint64_t n_break = (n_ids + kChainSeg - 1) / kChainSeg;
     for (uint64_t t = 0; t < trips; t++) {
-        const uint64_t k = first + t * stride;
+        // CHAIN: lanes 0 .. n_break-1 take the breakers (entries 0, kChainSeg, ...), the rest the other entries
+        const uint64_t g = first + t * stride;
+        const bool breaker = CHAIN && g < n_break;
+        const uint64_t k = !CHAIN ? g : breaker ? g * kChainSeg : (g - n_break) + (g - n_break) / (kChainSeg - 1) + 1;
         uint2 a = make_uint2(0xFFFFFFFFu, 0xFFFFFFFFu);
-        if (k < n_ids) {
-            const uint32_t id = ids[k];
-            const uint64_t slot = (uint64_t)id - id_base;
-            if (id >= id_base && slot < n_anchors) a = anchors[slot];
-        }
+        if (k < n_ids) a = survivor_anchor(anchors, n_anchors, id_base, ids, k);
         const bool inside = a.x < sq.Lr && a.y < sq.Lq;
+        uint32_t dL = 0, dR = 0;  // bases to the previous / next survivor on this diagonal (0: none)
+        if (CHAIN && inside) {
+            if (k > 0) {
+                const uint2 p = survivor_anchor(anchors, n_anchors, id_base, ids, k - 1);
+                if (p.x < sq.Lr && p.y < sq.Lq && p.x - p.y == a.x - a.y && p.y < a.y) dL = a.y - p.y;
+            }
+            if (k + 1 < n_ids) {
+                const uint2 q = survivor_anchor(anchors, n_anchors, id_base, ids, k + 1);
+                if (q.x < sq.Lr && q.y < sq.Lq && q.x - q.y == a.x - a.y && q.y > a.y) dR = q.y - a.y;
+            }
+        }
         WalkState w{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
         if (inside) {
             walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, 0);
@@ -194,9 +250,11 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
             w.q0 = __ldg(w.pq);
             w.q1 = __ldg(w.pq + 1);
         }
-        bool active = inside, stepping = inside, long_walk = false;
-        int side = 0, ML = 0, MR = 0;
+        bool active = inside, stepping = inside, long_walk = false, joined = false, jL = false;
+        int side = 0, ML = 0, MR = 0, CL = 0, CR = 0;
         uint32_t nL = 0, nR = 0, steps = 0;
+        // the first step whose end lies at least d pairs out (CHAIN joins are checked from there on)
+        uint32_t tjoin = (dL && !breaker) ? (dL - 1u) >> 3 : 0xFFFFFFFFu;
         int mstep = -1, mS = 0;  // the step in which the maximum last rose, and the sum at its start
         while (__any_sync(kFullMask, active)) {
 #pragma unroll
@@ -212,10 +270,13 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
                     m = max(m, Sv[j]);
                 }
                 const bool over = (d < 0) | (w.rem <= 8);
+                // a join: past the neighbour and standing at the running maximum
+                const bool join = CHAIN && stepping && !over && steps >= tjoin && m == Sv[7];
+                joined |= join;
                 const bool rose = stepping && m > w.M;
                 mstep = rose ? (int)steps : mstep;
                 mS = rose ? w.S : mS;
-                const bool adv = stepping && !over;
+                const bool adv = stepping && !over && !join;
                 w.M = stepping ? m : w.M;
                 stepping = adv;
                 steps += adv ? 1u : 0u;
@@ -236,7 +297,7 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
                 active = false;
             }
             if (active && !stepping) {
-                // the side is over: its maximum w.M, first reached in step mstep
+                // the side is over (or joined): its maximum w.M, first reached in step mstep
                 uint32_t nbest = 0;
                 if (mstep >= 0) {
                     const uint32_t back = steps - (uint32_t)mstep;
@@ -252,9 +313,29 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
                         if (Sm[j] == w.M) kk = j;
                     nbest = (uint32_t)mstep * 8u + (uint32_t)kk + 1u;
                 }
+                int Cs = 0;
+                if (CHAIN && joined) {  // the running sum after the first d pairs, scored again
+                    WalkState w0;
+                    walk_place(w0, sq, ref_rev, qry_rev, a.x, a.y, side);
+                    const uint32_t *pr = w0.pr, *pq = w0.pq;
+                    for (uint32_t left = side ? dR : dL; left;) {
+                        const uint32_t kk = min(left, 8u);
+                        int Sc[8];
+                        step_sums<true, HAS_N>(__funnelshift_r(__ldg(pr), __ldg(pr + 1), w0.shr),
+                                               __funnelshift_r(__ldg(pq), __ldg(pq + 1), w0.shq), low_nibbles(kk),
+                                               tlo, thi, tab, Cs, Sc);
+                        Cs = Sc[7];
+                        left -= kk;
+                        pr++;
+                        pq++;
+                    }
+                }
                 if (side == 0) {
                     ML = w.M;
                     nL = nbest;
+                    CL = Cs;
+                    jL = joined;
+                    joined = false;
                     side = 1;
                     walk_place(w, sq, ref_rev, qry_rev, a.x, a.y, 1);
                     w.r0 = __ldg(w.pr);
@@ -264,26 +345,37 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
                     mstep = -1;
                     mS = 0;
                     steps = 0;
+                    tjoin = (dR && !breaker) ? (dR - 1u) >> 3 : 0xFFFFFFFFu;
                     stepping = true;
                 } else {
                     MR = w.M;
                     nR = nbest;
+                    CR = Cs;
                     active = false;
                 }
             }
         }
         if (k >= n_ids) continue;
+        int64_t L = ML, Rt = MR;
+        if (inside && long_walk) {
+            uint64_t n0, n1;
+            side_exact(sq, tab, sa.xdrop, a.x, a.y, false, L, n0);
+            side_exact(sq, tab, sa.xdrop, a.x, a.y, true, Rt, n1);
+            nL = (uint32_t)n0;
+            nR = (uint32_t)n1;
+            joined = jL = false;
+        }
+        if (CHAIN && (dL | dR)) {  // a run member: k_chain_resolve settles it
+            info[k] = ChainInfo{(dR ? kLinkR : 0u) | (dL ? kLinkL : 0u) | (joined ? kJoinR : 0u) | (jL ? kJoinL : 0u),
+                                dR};
+            sR[k] = ChainSide{(long long)Rt, nR, CR};
+            sL[k] = ChainSide{(long long)L, nL, CL};
+            continue;
+        }
+        if (CHAIN) info[k] = ChainInfo{0u, 0u};
         uint4 rec = make_uint4(0, 0, 0, 0);
         uint8_t ok = 0;
         if (inside) {
-            int64_t L = ML, Rt = MR;
-            if (long_walk) {
-                uint64_t n0, n1;
-                side_exact(sq, tab, sa.xdrop, a.x, a.y, false, L, n0);
-                side_exact(sq, tab, sa.xdrop, a.x, a.y, true, Rt, n1);
-                nL = (uint32_t)n0;
-                nR = (uint32_t)n1;
-            }
             int64_t score = L + Rt;
             if (score > 2147483647LL) score = 2147483647LL;
             if (score >= sa.T) {
@@ -293,6 +385,103 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
         }
         out[k] = rec;
         done[k] = ok;
+    }
+}
+
+// Settles the linked survivors left by k_materialize_blocks<.., true>, one
+// warp per segment of kChainSeg = 32 entries, a lane per entry.  Right
+// sides: a joined side's maximum is C plus the next entry's maximum, so the
+// maxima are suffix sums of C, each closed by a side that did not join (past
+// the segment's end, the next breaker's right side closes them); a joined
+// side's position is d plus the next entry's position where C + that maximum
+// exceeds its own maximum at the join, else its own: suffix sums again.  Left
+// sides the same way as prefix sums (the segment's first entry is a breaker).
+// Each linked entry's record is written.
+template <typename V>
+__device__ __forceinline__ V seg_suffix_sum(V v, bool open, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const V v2 = __shfl_down_sync(kFullMask, v, off);
+        const bool o2 = __shfl_down_sync(kFullMask, open, off);
+        if (open && lane + off < 32) {
+            v += v2;
+            open = o2;
+        }
+    }
+    return v;
+}
+
+template <typename V>
+__device__ __forceinline__ V seg_prefix_sum(V v, bool open, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const V v2 = __shfl_up_sync(kFullMask, v, off);
+        const bool o2 = __shfl_up_sync(kFullMask, open, off);
+        if (open && lane >= off) {
+            v += v2;
+            open = o2;
+        }
+    }
+    return v;
+}
+
+// Whether an entry's suffix sum runs past the segment's end: every entry from
+// it to the last lane is open.
+__device__ __forceinline__ bool open_to_end(bool open, int lane) {
+    const unsigned closed = __ballot_sync(kFullMask, !open);
+    return (closed >> lane) == 0u;
+}
+
+__global__ void __launch_bounds__(256) k_chain_resolve(const uint2 *__restrict__ anchors, uint64_t n_anchors,
+                                                       uint32_t id_base, const uint32_t *__restrict__ ids,
+                                                       uint64_t n_ids, const uint64_t *__restrict__ d_n, int32_t T,
+                                                       const ChainSide *__restrict__ sR,
+                                                       const ChainSide *__restrict__ sL,
+                                                       const ChainInfo *__restrict__ info, uint4 *__restrict__ out,
+                                                       uint8_t *__restrict__ done) {
+    if (d_n) n_ids = *d_n <= n_ids ? *d_n : 0;
+    const int lane = threadIdx.x & 31;
+    const uint64_t n_seg = (n_ids + kChainSeg - 1) / kChainSeg;
+    const uint64_t n_warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
+    for (uint64_t sg = ((uint64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; sg < n_seg; sg += n_warps) {
+        const uint64_t j = sg * kChainSeg + lane;
+        const uint64_t last = min(sg * kChainSeg + kChainSeg, n_ids) - 1;
+        const ChainInfo f = j < n_ids ? info[j] : ChainInfo{0u, 0u};
+        const bool member = (f.flags & (kLinkR | kLinkL)) != 0;
+        const ChainSide zero{0, 0u, 0};
+        const ChainSide r = member ? sR[j] : zero, l = member ? sL[j] : zero;
+        // the side after the segment: the next breaker's, when the last entry links to it
+        long long Mc = 0;
+        uint32_t nc = 0;
+        if (last + 1 < n_ids && (info[last].flags & kLinkR)) {
+            Mc = sR[last + 1].M;
+            nc = sR[last + 1].n;
+        }
+        // right maxima and positions
+        const bool jr = (f.flags & kJoinR) != 0;
+        long long MR = seg_suffix_sum<long long>(jr ? (long long)r.C : r.M, jr, lane);
+        if (open_to_end(jr, lane)) MR += Mc;
+        const bool cr = jr && MR > r.M;
+        uint32_t nR = seg_suffix_sum<uint32_t>(cr ? f.dR : r.n, cr, lane);
+        if (open_to_end(cr, lane)) nR += nc;
+        // left maxima and positions (an entry's left distance is the previous entry's dR)
+        const bool jl = (f.flags & kJoinL) != 0;
+        const long long ML = seg_prefix_sum<long long>(jl ? (long long)l.C : l.M, jl, lane);
+        const uint32_t dL = __shfl_up_sync(kFullMask, f.dR, 1);
+        const bool cl = jl && ML > l.M;
+        const uint32_t nL = seg_prefix_sum<uint32_t>(cl ? dL : l.n, cl, lane);
+        if (!member) continue;
+        const uint2 a = survivor_anchor(anchors, n_anchors, id_base, ids, j);
+        long long score = ML + MR;
+        if (score > 2147483647LL) score = 2147483647LL;
+        uint4 rec = make_uint4(0, 0, 0, 0);
+        uint8_t ok = 0;
+        if (score >= T) {
+            rec = make_uint4(a.x - nL, a.y - nL, nL + nR - 1u, (uint32_t)(int32_t)score);
+            ok = 1;
+        }
+        out[j] = rec;
+        done[j] = ok;
     }
 }
 
@@ -342,10 +531,32 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
         const uint64_t blocks = (n_ids + 255) / 256;
         const unsigned g = (unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64);
         const bool has_n = ref.has_n || qry.has_n;
-        auto kern = sa.exact ? (has_n ? k_materialize_blocks<true> : k_materialize_blocks<false>)
-                             : (has_n ? k_materialize_lane<true> : k_materialize_lane<false>);
-        kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa, out,
-                                d_done); count_launch();
+        if (sa.exact && kMaterializeChain) {
+            // walks join their diagonal neighbours' walks; the runs are settled after
+            void *scratch = nullptr;
+            cudaError_t e = pool_alloc(&scratch, n_ids * (2 * sizeof(ChainSide) + sizeof(ChainInfo)), st);
+            if (e != cudaSuccess) return e;
+            ChainSide *sR = reinterpret_cast<ChainSide *>(scratch), *sL = sR + n_ids;
+            ChainInfo *info = reinterpret_cast<ChainInfo *>(sL + n_ids);
+            auto kern = has_n ? k_materialize_blocks<true, true> : k_materialize_blocks<false, true>;
+            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
+                                    out, d_done, sR, sL, info); count_launch();
+            const uint64_t segs = (n_ids + kChainSeg - 1) / kChainSeg, sb = (segs + 7) / 8;  // a warp per segment
+            k_chain_resolve<<<(unsigned)(sb < 152ull * 64 ? sb : 152ull * 64), 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, sa.T, sR, sL, info, out,
+                                               d_done); count_launch();
+            e = cudaGetLastError();
+            const cudaError_t ef = pool_free(scratch, st);
+            return e != cudaSuccess ? e : ef;
+        }
+        if (sa.exact) {
+            auto kern = has_n ? k_materialize_blocks<true, false> : k_materialize_blocks<false, false>;
+            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
+                                    out, d_done, nullptr, nullptr, nullptr); count_launch();
+        } else {
+            auto kern = has_n ? k_materialize_lane<true> : k_materialize_lane<false>;
+            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
+                                    out, d_done); count_launch();
+        }
     } else {
         k_materialize<<<grid_cap(n_ids, 128), 128, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry),
                                                                     sa, out, d_done); count_launch();

@@ -346,3 +346,48 @@ def test_process_chunk_capacity_and_counts(torch_cuda):
     assert np.array_equal(big[1].cpu().numpy(), orc["rec"])
     assert np.array_equal(big[2].cpu().numpy(), orc["done"])
     assert np.array_equal(big[3][:na].cpu().numpy().view(np.uint32), orc["accepted"])
+
+
+def test_materialize_any_id_order(torch_cuda):
+    """E.1-E.5 per survivor, whatever the id list: ascending survivors (long
+    runs of neighbours on one diagonal), reversed, shuffled, with duplicates,
+    with ids outside the anchors, every anchor of a chunk, and lists cut so
+    that runs start and end at every place.  Each record must equal the
+    oracle's record for that id alone."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    rng = np.random.default_rng(23)
+    m = synth.hoxd70()
+    s = rng.integers(0, 4, 6000).astype(np.uint8)
+    ref = s.copy()
+    ref[2500:2510] = 4                        # N inside the long diagonal
+    qry = np.concatenate([s[1000:4000], rng.integers(0, 4, 500).astype(np.uint8), s[4000:5200]])
+    qry[rng.random(qry.size) < 0.06] = rng.integers(0, 4, 1).astype(np.uint8)
+    w = synth.make("tiny")
+    for r, q in ((ref, qry), (w.ref, w.query)):
+        eng = _engine(torch, r, m, 910, 3000)
+        plan = eng.plan(_dev(torch, q))
+        n = plan.total_hits
+        anchors = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+        flags = torch.empty(n, dtype=torch.uint8, device="cuda")
+        hspz.hspz_expand_gate(plan, 0, eng.params, anchors, flags)
+        a_np = anchors.cpu().numpy().view(np.uint32)
+        surv = np.nonzero(flags.cpu().numpy())[0].astype(np.int64)
+        base = 77
+        lists = [surv, surv[::-1], rng.permutation(surv), np.repeat(surv[:300], 2),
+                 np.arange(n), np.concatenate([surv[:50], [n + 5, n + 6], surv[50:120], [0], surv[120:]])]
+        lists += [surv[c:] for c in (1, 7, 131)] + [surv[:c] for c in (1, 2, 9, 200)]
+        for ids_local in lists:
+            ids = (np.asarray(ids_local, np.int64) + base).astype(np.uint32)
+            k = ids.size
+            d_ids = torch.from_numpy(ids.view(np.int32)).cuda()
+            out = torch.full((max(k, 1), 4), -3, dtype=torch.int32, device="cuda")
+            done = torch.full((max(k, 1),), 9, dtype=torch.uint8, device="cuda")
+            hspz.hspz_materialize(eng.index, plan, anchors, base, d_ids, k, eng.params, out, done)
+            # an id outside the anchors gets an empty record (the oracle takes valid ids only)
+            valid = np.asarray(ids_local, np.int64) < n
+            rec_o = np.zeros((k, 4), np.int32)
+            done_o = np.zeros(k, np.uint8)
+            rec_o[valid], done_o[valid] = oracle.materialize(r, q, a_np, base, ids[valid], m, 910, 3000)
+            assert np.array_equal(done[:k].cpu().numpy(), done_o)
+            assert np.array_equal(out[:k].cpu().numpy(), rec_o)
