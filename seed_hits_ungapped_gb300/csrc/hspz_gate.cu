@@ -206,8 +206,16 @@ __device__ __forceinline__ bool gate_side(WalkState &w, bool walk, uint32_t tlo,
     if (EXACT) {
         constexpr int lead = BACK ? kLeadLeft : kLeadRight;
         if (!walk) w.rem = 0;
+        if (__all_sync(kFullMask, w.rem == 0u || w.rem > 8u * lead)) {
+            // no walk of the round can reach its edge during the lead steps
+            uint32_t keep = w.rem ? 0xFFFFFFFFu : 0u;
 #pragma unroll
-        for (int i = 0; i < lead; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
+            for (int i = 0; i < lead; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
+            w.rem = keep ? w.rem - 8u * lead : 0u;
+        } else {
+#pragma unroll
+            for (int i = 0; i < lead; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
+        }
         // the tail: the same steps under a warp vote, while any lane walks
         while (__any_sync(kFullMask, w.rem != 0)) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
         return walk && w.M >= need;

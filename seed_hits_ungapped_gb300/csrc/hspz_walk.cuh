@@ -270,6 +270,47 @@ __device__ __forceinline__ void walk_step_lead(WalkState &w, uint32_t tlo, uint3
     }
 }
 
+// walk_step_lead for a walk that cannot reach its sequence edge during the
+// step: the step's bases are all inside, so the keep mask is all or nothing
+// (`keep`: ~0 while the side walks, 0 once it is over) and rem is neither
+// read nor changed.
+template <bool HAS_N, bool BACK>
+__device__ __forceinline__ void walk_step_inner(WalkState &w, uint32_t &keep, uint32_t tlo, uint32_t thi,
+                                                const int *__restrict__ tab25, int X, int need) {
+    const uint32_t R = __funnelshift_r(w.r0, w.r1, w.shr);
+    const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
+    int Sv[8];
+    step_sums<!BACK, HAS_N>(R, Q, keep, tlo, thi, tab25, w.S, Sv);
+    int m = w.M, d = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k++) {
+        d |= Sv[k] + X - m;
+        m = max(m, Sv[k]);
+    }
+    w.M = m;
+    w.S = Sv[7];
+    keep = ((d | (need - 1 - m)) < 0) ? 0u : keep;
+    if (BACK) {
+        w.r1 = w.r0;
+        w.q1 = w.q0;
+        w.pr--;
+        w.pq--;
+        if (keep) {
+            w.r0 = __ldg(w.pr);
+            w.q0 = __ldg(w.pq);
+        }
+    } else {
+        w.r0 = w.r1;
+        w.q0 = w.q1;
+        w.pr++;
+        w.pq++;
+        if (keep) {
+            w.r1 = __ldg(w.pr + 1);
+            w.q1 = __ldg(w.pq + 1);
+        }
+    }
+}
+
 // Exact side walk with the earliest maximum (E.2/E.3).  64-bit sums.
 __device__ __forceinline__ void side_exact(const Seqs &s, const int *__restrict__ tab, int64_t X, uint32_t ar,
                                            uint32_t aq, bool right, int64_t &best, uint64_t &best_n) {
