@@ -175,6 +175,15 @@ __global__ void __launch_bounds__(256) k_materialize_lane(const uint2 *__restric
 constexpr bool kMaterializeChain = HSPZ_MATERIALIZE_CHAIN != 0;
 constexpr uint32_t kLinkR = 1, kLinkL = 2, kJoinR = 4, kJoinL = 8;
 constexpr uint64_t kChainSeg = 32;  // one warp settles a segment
+constexpr uint64_t kChainSlice = 1ull << 25;  // ids per launch pair: 1.3 GB of scratch at most
+
+// Entries of a slice [n_off, n_off + cap) of an id list of capacity n_total
+// whose live length (*d_n) is known on the device only; a live length above
+// the capacity means nothing is materialized (the caller reports it).
+__device__ __forceinline__ uint64_t live_count(uint64_t live, uint64_t n_off, uint64_t cap, uint64_t n_total) {
+    if (live > n_total || live <= n_off) return 0;
+    return live - n_off < cap ? live - n_off : cap;
+}
 struct ChainSide {
     long long M;  // the side maximum, or the running sum (and maximum) at the join
     uint32_t n;   // pairs out to the earliest base of that maximum
@@ -206,7 +215,8 @@ constexpr int kMatBlock = 8;
 template <bool HAS_N, bool CHAIN>
 __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                             uint32_t id_base, const uint32_t *__restrict__ ids,
-                                                            uint64_t n_ids, const uint64_t *__restrict__ d_n, Seqs sq,
+                                                            uint64_t n_ids, const uint64_t *__restrict__ d_n,
+                                                            uint64_t n_off, uint64_t n_total, Seqs sq,
                                                             const uint32_t *__restrict__ ref_rev,
                                                             const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
                                                             uint4 *__restrict__ out, uint8_t *__restrict__ done,
@@ -218,7 +228,7 @@ __global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restr
     const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
     const int X = sa.xdrop;
     const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
-    if (d_n) n_ids = *d_n <= n_ids ? *d_n : 0;
+    if (d_n) n_ids = live_count(*d_n, n_off, n_ids, n_total);
     // the grid-stride loop runs the same number of trips in every lane of a warp
     const uint64_t first = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x;
     const uint64_t trips = (n_ids + stride - 1) / stride;
@@ -434,12 +444,13 @@ __device__ __forceinline__ bool open_to_end(bool open, int lane) {
 
 __global__ void __launch_bounds__(256) k_chain_resolve(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                        uint32_t id_base, const uint32_t *__restrict__ ids,
-                                                       uint64_t n_ids, const uint64_t *__restrict__ d_n, int32_t T,
+                                                       uint64_t n_ids, const uint64_t *__restrict__ d_n,
+                                                       uint64_t n_off, uint64_t n_total, int32_t T,
                                                        const ChainSide *__restrict__ sR,
                                                        const ChainSide *__restrict__ sL,
                                                        const ChainInfo *__restrict__ info, uint4 *__restrict__ out,
                                                        uint8_t *__restrict__ done) {
-    if (d_n) n_ids = *d_n <= n_ids ? *d_n : 0;
+    if (d_n) n_ids = live_count(*d_n, n_off, n_ids, n_total);
     const int lane = threadIdx.x & 31;
     const uint64_t n_seg = (n_ids + kChainSeg - 1) / kChainSeg;
     const uint64_t n_warps = (uint64_t)gridDim.x * (blockDim.x >> 5);
@@ -532,26 +543,33 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
         const unsigned g = (unsigned)(blocks < 152ull * 64 ? blocks : 152ull * 64);
         const bool has_n = ref.has_n || qry.has_n;
         if (sa.exact && kMaterializeChain) {
-            // walks join their diagonal neighbours' walks; the runs are settled after
+            // walks join their diagonal neighbours' walks and the joins are settled after;
+            // slices of at most kChainSlice ids bound the scratch (no link crosses a slice)
+            const uint64_t slice = n_ids < kChainSlice ? n_ids : kChainSlice;
             void *scratch = nullptr;
-            cudaError_t e = pool_alloc(&scratch, n_ids * (2 * sizeof(ChainSide) + sizeof(ChainInfo)), st);
+            cudaError_t e = pool_alloc(&scratch, slice * (2 * sizeof(ChainSide) + sizeof(ChainInfo)), st);
             if (e != cudaSuccess) return e;
-            ChainSide *sR = reinterpret_cast<ChainSide *>(scratch), *sL = sR + n_ids;
-            ChainInfo *info = reinterpret_cast<ChainInfo *>(sL + n_ids);
+            ChainSide *sR = reinterpret_cast<ChainSide *>(scratch), *sL = sR + slice;
+            ChainInfo *info = reinterpret_cast<ChainInfo *>(sL + slice);
             auto kern = has_n ? k_materialize_blocks<true, true> : k_materialize_blocks<false, true>;
-            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
-                                    out, d_done, sR, sL, info); count_launch();
-            const uint64_t segs = (n_ids + kChainSeg - 1) / kChainSeg, sb = (segs + 7) / 8;  // a warp per segment
-            k_chain_resolve<<<(unsigned)(sb < 152ull * 64 ? sb : 152ull * 64), 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, sa.T, sR, sL, info, out,
-                                               d_done); count_launch();
-            e = cudaGetLastError();
+            const uint64_t segs = (slice + kChainSeg - 1) / kChainSeg, sb = (segs + 7) / 8;  // a warp per segment
+            const unsigned gs = (unsigned)((slice + 255) / 256 < 152ull * 64 ? (slice + 255) / 256 : 152ull * 64);
+            const unsigned gr = (unsigned)(sb < 152ull * 64 ? sb : 152ull * 64);
+            for (uint64_t off = 0; off < n_ids && e == cudaSuccess; off += slice) {
+                const uint64_t len = n_ids - off < slice ? n_ids - off : slice;
+                kern<<<gs, 256, 0, st>>>(an, n_anchors, id_base, d_ids + off, len, d_n, off, n_ids, seqs(ref, qry), ref.rev,
+                                         qry.rev, sa, out + off, d_done + off, sR, sL, info); count_launch();
+                k_chain_resolve<<<gr, 256, 0, st>>>(an, n_anchors, id_base, d_ids + off, len, d_n, off, n_ids, sa.T, sR, sL,
+                                                    info, out + off, d_done + off); count_launch();
+                e = cudaGetLastError();
+            }
             const cudaError_t ef = pool_free(scratch, st);
             return e != cudaSuccess ? e : ef;
         }
         if (sa.exact) {
             auto kern = has_n ? k_materialize_blocks<true, false> : k_materialize_blocks<false, false>;
-            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
-                                    out, d_done, nullptr, nullptr, nullptr); count_launch();
+            kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, 0, n_ids, seqs(ref, qry), ref.rev, qry.rev,
+                                    sa, out, d_done, nullptr, nullptr, nullptr); count_launch();
         } else {
             auto kern = has_n ? k_materialize_lane<true> : k_materialize_lane<false>;
             kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,
