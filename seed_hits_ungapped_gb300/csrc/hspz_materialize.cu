@@ -212,8 +212,11 @@ __device__ __forceinline__ uint2 survivor_anchor(const uint2 *__restrict__ ancho
 // links in info for k_chain_resolve, every other survivor gets its record.
 constexpr int kMatBlock = 8;
 
+#ifndef HSPZ_MAT_MIN_BLOCKS
+#define HSPZ_MAT_MIN_BLOCKS 4
+#endif
 template <bool HAS_N, bool CHAIN>
-__global__ void __launch_bounds__(256) k_materialize_blocks(const uint2 *__restrict__ anchors, uint64_t n_anchors,
+__global__ void __launch_bounds__(256, HSPZ_MAT_MIN_BLOCKS) k_materialize_blocks(const uint2 *__restrict__ anchors, uint64_t n_anchors,
                                                             uint32_t id_base, const uint32_t *__restrict__ ids,
                                                             uint64_t n_ids, const uint64_t *__restrict__ d_n,
                                                             uint64_t n_off, uint64_t n_total, Seqs sq,
