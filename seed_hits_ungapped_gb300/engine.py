@@ -2,7 +2,9 @@
 
 ``HspEngine`` owns a reference index and reusable device buffers; ``run``
 takes one query batch (a CUDA uint8 tensor) and, per MAX_HITS chunk, calls
-hspz_expand_gate -> hspz_compact -> hspz_materialize -> hspz_compact (accepted).
+hspz_expand_gate -> hspz_compact -> hspz_materialize -> hspz_compact (accepted);
+``run_stream`` takes batches in host memory and overlaps their copies with
+the compute of neighbouring batches.
 Every step runs in libhspz; this module only allocates torch buffers and
 passes pointers.
 """
@@ -107,16 +109,17 @@ class HspEngine:
             return torch.cuda.ExternalStream(self.stream)
         return self.stream
 
-    def _host_rows(self, name: str, k: int, n: int, dtype, cols: int = 1):
+    def _host_rows(self, name: str, k: int, n: int, dtype, cols: int = 1, stream=None):
         """Room for n more rows after the first k of a pinned host buffer
-        (grown geometrically; the first k rows are kept)."""
+        (grown geometrically; the first k rows are kept).  `stream`: the
+        stream whose copies may still land in it (default: the engine's)."""
         torch = self.torch
         have = self._host_bufs.get(name)
         if have is None or have.shape[0] < k + n:
             rows = max(k + n, int(1.5 * have.shape[0]) if have is not None else 0, 1024)
             new = torch.empty((rows, cols) if cols > 1 else (rows,), dtype=dtype, pin_memory=True)
             if have is not None and k:
-                self._torch_stream().synchronize()  # copies still landing in the old buffer
+                (stream or self._torch_stream()).synchronize()  # copies still landing in the old buffer
                 new[:k].copy_(have[:k])
             self._host_bufs[name] = new
         return self._host_bufs[name]
@@ -148,18 +151,20 @@ class HspEngine:
     def plan(self, d_query, max_hits: int = 0, walk_full: bool = False):
         return hspz.hspz_find_hits(self.index, d_query, max_hits, walk_full, stream=self.stream)
 
-    def process_chunk(self, plan, c: int, time_gate: bool = False):
+    def process_chunk(self, plan, c: int, time_gate: bool = False, bufset: str = ""):
         """hspz_process_chunk on the engine's buffers, growing the survivor
         buffers and running the chunk again when they are too small.
+        `bufset` names a separate set of survivor / result buffers.
         Returns (n_anchors, n_survivors, n_accepted, gate_ms)."""
         torch = self.torch
         n = int(plan.chunks[c, 3]) - int(plan.chunks[c, 2])
         anchors = self.buffer("anchors", n, torch.int32, 2)
         flags = self.buffer("flags", n, torch.uint8)
-        cap = self._bufs["ids"].shape[0] if "ids" in self._bufs else max(1024, n // 32)
+        ids_name = "ids" + bufset
+        cap = self._bufs[ids_name].shape[0] if ids_name in self._bufs else max(1024, n // 32)
         while True:
-            bufs = [self.buffer("ids", cap, torch.int32), self.buffer("records", cap, torch.int32, 4),
-                    self.buffer("done", cap, torch.uint8), self.buffer("accepted", cap, torch.int32)]
+            bufs = [self.buffer(ids_name, cap, torch.int32), self.buffer("records" + bufset, cap, torch.int32, 4),
+                    self.buffer("done" + bufset, cap, torch.uint8), self.buffer("accepted" + bufset, cap, torch.int32)]
             try:
                 ns, na, ms = hspz.hspz_process_chunk(plan, c, self.params, anchors, flags, *bufs,
                                                      stream=self.stream, time_gate=time_gate)
@@ -235,4 +240,99 @@ class HspEngine:
             if keep:
                 res.final_idx = _np_u32(ids[:n_final]).copy()
         plan.close()
+        return res
+
+    def run_stream(self, host_queries, max_hits: int = 0):
+        """Query batches from host memory through the whole path, pipelined.
+
+        `host_queries` is an iterable of uint8 CPU tensors (pinned, for the
+        copies to overlap).  While the compute stream works on batch i, a
+        copy stream brings batch i+1 to the device and takes each finished
+        chunk's results (records, done flags, accepted ids) back to pinned
+        host buffers.  Yields one BatchResult per batch, in order, once its
+        results are on the host; its arrays stay valid until the generator is
+        resumed.  Device query and result buffers alternate between two sets,
+        so a set is reused only after its copies have finished (events on the
+        streams)."""
+        torch = self.torch
+        ks = self._torch_stream()
+        cs = getattr(self, "_copy_stream", None)
+        if cs is None:
+            cs = self._copy_stream = torch.cuda.Stream()
+        dq = [None, None]
+        ev_in = [None, None]
+
+        def upload(q, p):
+            n = q.numel()
+            have = dq[p]
+            if have is None or have.numel() < n:
+                dq[p] = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
+            with torch.cuda.stream(cs):
+                dq[p][:n].copy_(q, non_blocking=True)
+                ev_in[p] = torch.cuda.Event()
+                ev_in[p].record(cs)
+            return n
+
+        it = iter(host_queries)
+        q = next(it, None)
+        if q is None:
+            return
+        n_cur = upload(q, 0)
+        ev_out = [None, None]  # per result set: the copies of the last chunk that used it
+        n_chunk = 0
+        pending = None
+        i = 0
+        while q is not None:
+            p = i & 1
+            ks.wait_event(ev_in[p])
+            plan = self.plan(dq[p][:n_cur], max_hits)  # reads the query, then the host waits for it
+            dq[p].record_stream(ks)
+            q = next(it, None)
+            n_next = upload(q, 1 - p) if q is not None else 0  # the other buffer's batch is planned
+            out, views, off_s, off_a = [], [], 0, 0
+            for c in range(plan.n_chunks):
+                r_set = n_chunk & 1
+                if ev_out[r_set] is not None:
+                    ks.wait_event(ev_out[r_set])
+                n, n_surv, n_acc, _ = self.process_chunk(plan, c, bufset="_s%d" % r_set)
+                r = ChunkResult(int(plan.chunks[c, 2]), n, n_surv, n_acc)
+                rec, done, acc = (self._bufs[k + "_s%d" % r_set] for k in ("records", "done", "accepted"))
+                h_rec = self._host_rows("records_h%d" % p, off_s, n_surv, torch.int32, 4, stream=cs)
+                h_done = self._host_rows("done_h%d" % p, off_s, n_surv, torch.uint8, stream=cs)
+                h_acc = self._host_rows("accepted_h%d" % p, off_a, n_acc, torch.int32, stream=cs)
+                ev_k = torch.cuda.Event()
+                ev_k.record(ks)
+                cs.wait_event(ev_k)
+                with torch.cuda.stream(cs):
+                    h_rec[off_s:off_s + n_surv].copy_(rec[:n_surv], non_blocking=True)
+                    h_done[off_s:off_s + n_surv].copy_(done[:n_surv], non_blocking=True)
+                    h_acc[off_a:off_a + n_acc].copy_(acc[:n_acc], non_blocking=True)
+                    ev_out[r_set] = torch.cuda.Event()
+                    ev_out[r_set].record(cs)
+                for t in (rec, done, acc):
+                    t.record_stream(cs)
+                views.append((r, off_s, n_surv, off_a, n_acc))
+                out.append(r)
+                off_s += n_surv
+                off_a += n_acc
+                n_chunk += 1
+            res = BatchResult(plan.n_seeds, plan.total_hits, plan.chunks.copy(), out)
+            plan.close()
+            last = torch.cuda.Event()
+            last.record(cs)
+            if pending is not None:
+                yield self._finish_stream(*pending)
+            pending = (res, views, last, p)
+            n_cur = n_next
+            i += 1
+        yield self._finish_stream(*pending)
+
+    def _finish_stream(self, res, views, ev, p):
+        """Waits for a streamed batch's result copies and attaches host views."""
+        ev.synchronize()
+        h_rec, h_done, h_acc = (self._host_bufs[k + "_h%d" % p] for k in ("records", "done", "accepted"))
+        for r, os_, ns_, oa, na in views:
+            r.records = h_rec[os_:os_ + ns_].numpy()
+            r.done = h_done[os_:os_ + ns_].numpy()
+            r.accepted = h_acc[oa:oa + na].numpy().view(np.uint32)
         return res

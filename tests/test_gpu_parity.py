@@ -391,3 +391,28 @@ def test_materialize_any_id_order(torch_cuda):
             rec_o[valid], done_o[valid] = oracle.materialize(r, q, a_np, base, ids[valid], m, 910, 3000)
             assert np.array_equal(done[:k].cpu().numpy(), done_o)
             assert np.array_equal(out[:k].cpu().numpy(), rec_o)
+
+
+def test_run_stream_batches_match_oracle(torch_cuda):
+    """HspEngine.run_stream: uploads and result copies on a copy stream,
+    overlapping the next batch.  Every batch, chunk by chunk, must hold the
+    oracle's records, done flags and accepted ids; several chunks per batch
+    (MAX_HITS cuts) make the two result sets alternate within a batch."""
+    torch = torch_cuda
+    w = synth.make("tiny")
+    m = w.matrix
+    eng = _engine(torch, w.ref, m, w.xdrop, w.K)
+    qs = [w.query, w.query[:60_000].copy(), w.query[:12].copy(), w.query[::-1].copy(), w.query[100_000:].copy()]
+    pinned = [torch.from_numpy(np.ascontiguousarray(q)).pin_memory() for q in qs]
+    for max_hits in (0, 4000):
+        got = 0
+        for q, res in zip(qs, eng.run_stream(pinned, max_hits=max_hits)):
+            orc = oracle.run_path(w.ref, q, m, w.xdrop, w.K, max_hits=max_hits)
+            assert res.total_hits == orc["total"]
+            assert len(res.per_chunk) == len(orc["per_chunk"])
+            for g, o in zip(res.per_chunk, orc["per_chunk"]):
+                assert np.array_equal(g.records, o["rec"])
+                assert np.array_equal(g.done, o["done"])
+                assert np.array_equal(g.accepted, o["accepted"])
+            got += 1
+        assert got == len(qs)
