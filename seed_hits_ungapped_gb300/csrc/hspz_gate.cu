@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
                 pend = cached ? sP[l] : __ldg(P + first + l);
                 base = __ldg(lo + first + l);
             }
-            sA[i0 + k] = make_uint2(__ldg(pos + base + (pend - 1 - g)), first + l + span - 1);
+            sA[i0 + k] = make_uint2(__ldcs(pos + base + (pend - 1 - g)), first + l + span - 1);
         }
     }
     __syncwarp();
@@ -369,10 +369,12 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
         uint2 a = make_uint2(0, 0);
         if (valid) a = sA[ai];
         const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, tlo, thi, tab, X, T);
-        if (valid) flags[t0 + ai] = accepted ? 1 : 0;
+        if (valid) __stcs(flags + t0 + ai, (uint8_t)(accepted ? 1 : 0));
     }
     // 3. anchors
-    for (uint32_t i = lane; i < count; i += 32) out[t0 + i] = sA[i];
+    // positions, flags and anchors stream through once (cache-streaming loads and stores),
+    // so the packed sequences the walks read stay in L2
+    for (uint32_t i = lane; i < count; i += 32) __stcs(out + t0 + i, sA[i]);
 }
 
 // Round-based fast gate over an anchor array in global memory (the standalone
