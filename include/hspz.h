@@ -269,7 +269,12 @@ uint64_t hspz_compact_noalloc_max_flags(void);
  * len = n_left + n_right - 1 (closed interval start..=start+len) and
  * score = M_left + M_right (saturated at INT32_MAX).  done[k] = score >= T: an
  * accepted slot holds the record, a rejected slot is written as zeros with
- * done = 0.  d_out must be 16-byte aligned.
+ * done = 0.  d_out must be 16-byte aligned.  Any order of d_ids is allowed;
+ * when the next entry is the next survivor on the same diagonal the two walks
+ * share work (same records).  When the 8-base stop test is exact (xdrop >= 7
+ * x the largest pair score) it uses stream-ordered scratch of 48 bytes per id
+ * (at most 2^25 ids at a time) from the library's memory pool; it does not
+ * synchronize `stream`.
  * ------------------------------------------------------------------------ */
 int hspz_materialize(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors,
                      uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
