@@ -280,6 +280,22 @@ int hspz_materialize(const hspz_index *index, const hspz_plan *plan, const hspz_
                      uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
                      const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * hspz_materialize with the ids taken in diagonal order: the same records and
+ * done flags, at the same places, for any id list.  Each slice of at most
+ * 2^25 ids is sorted (stable radix sort) by the anchor's diagonal
+ * (reference end - query end) first, so that survivors on one diagonal
+ * become neighbours and share their walks (hspz_materialize shares work only
+ * between neighbouring entries of the list).  Worth it when many survivors
+ * lie on the same diagonals but apart in the list, as in repeats: the ids of
+ * one query position hit many reference positions, i.e. many diagonals.
+ * Uses stream-ordered scratch of about 68 bytes per id (per slice) from the
+ * library's memory pool; does not synchronize `stream`.
+ * ------------------------------------------------------------------------ */
+int hspz_materialize_grouped(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors,
+                             uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
+                             const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
+
 /* ------------------------------------------------------------------------ *
  * Record gather: d_out[k] = d_records[d_idx[k]] for k < n (16-byte records;
  * both arrays 16-byte aligned; every d_idx[k] must index d_records).  Collects

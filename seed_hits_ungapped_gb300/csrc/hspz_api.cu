@@ -654,6 +654,21 @@ int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize");
 }
 
+int hspz_materialize_grouped(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors,
+                             uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
+                             const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done,
+                             void *stream) {
+    if (!ix || !p || p->index != ix) return HSPZ_E_INVAL;
+    if (n_ids && (!d_anchors || !d_ids || !d_out || !d_done)) return HSPZ_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
+    cudaError_t e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done,
+                                       (cudaStream_t)stream, nullptr, true);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize_grouped");
+}
+
 int hspz_chunk_walk_host(const uint32_t *prefix, uint64_t n_seeds, uint64_t max_hits, int use_block_sums,
                          hspz_chunk *chunks, uint32_t cap, uint32_t *n_chunks) {
     if (!n_chunks || (n_seeds && !prefix)) return HSPZ_E_INVAL;

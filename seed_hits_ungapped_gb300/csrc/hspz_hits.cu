@@ -408,6 +408,37 @@ cudaError_t launch_scan_u64(const uint64_t *d_in, uint64_t n, uint64_t *d_excl, 
     return launch_scan<uint64_t, uint64_t>(d_in, n, d_excl, d_incl, d_total, st);
 }
 
+uint64_t radix_sort_scratch_words(uint64_t n) {
+    const uint64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
+    return 2 * n + n_tiles * 256;
+}
+
+cudaError_t launch_radix_sort_pairs(uint32_t *d_keys, uint32_t *d_vals, uint64_t n, int key_bits, uint32_t *d_scratch,
+                                    cudaStream_t st) {
+    if (!n) return cudaSuccess;
+    const uint64_t n_tiles = (n + kRadixTile - 1) / kRadixTile;
+    uint32_t *k0 = d_keys, *v0 = d_vals, *k1 = d_scratch, *v1 = d_scratch + n, *hist = d_scratch + 2 * n;
+    const int smem = kRadixThreads * 256 * 2;
+    cudaError_t e = cudaFuncSetAttribute(k_radix_scatter, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int passes = 0;
+    for (int shift = 0; shift < key_bits && e == cudaSuccess; shift += 8, passes++) {
+        k_radix_hist<<<(unsigned)n_tiles, kRadixThreads, 0, st>>>(k0, n, shift, hist, n_tiles); count_launch();
+        e = cudaGetLastError();
+        if (e == cudaSuccess) e = launch_scan_u32(hist, n_tiles * 256, hist, st);
+        if (e != cudaSuccess) break;
+        k_radix_scatter<<<(unsigned)n_tiles, kRadixThreads, smem, st>>>(k0, v0, n, shift, hist, n_tiles, k1, v1); count_launch();
+        e = cudaGetLastError();
+        uint32_t *t = k0; k0 = k1; k1 = t;
+        t = v0; v0 = v1; v1 = t;
+    }
+    // an odd number of passes leaves the result in the scratch halves
+    if (e == cudaSuccess && (passes & 1)) {
+        e = cudaMemcpyAsync(d_keys, k0, n * 4, cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess) e = cudaMemcpyAsync(d_vals, v0, n * 4, cudaMemcpyDeviceToDevice, st);
+    }
+    return e;
+}
+
 cudaError_t launch_scan_u32(const uint32_t *d_in, uint64_t n, uint32_t *d_excl, cudaStream_t st) {
     return launch_scan<uint32_t, uint32_t>(d_in, n, d_excl, (uint32_t *)nullptr, (uint32_t *)nullptr, st);
 }

@@ -98,11 +98,16 @@ uint64_t bucket_scratch_words(uint64_t n, uint32_t n_buckets);
 cudaError_t launch_bucket_sort(const hspz_anchor *d_anchors, uint64_t n, uint32_t span, uint32_t n_buckets,
                                hspz_anchor *d_sorted, uint32_t *d_raw, uint32_t *d_scratch, cudaStream_t st);
 cudaError_t launch_scan_u32(const uint32_t *d_in, uint64_t n, uint32_t *d_excl, cudaStream_t st);
+// Stable LSD radix sort of n (key, value) pairs by the low key_bits bits of the
+// key (8 bits per pass), in place; scratch of radix_sort_scratch_words(n) words.
+uint64_t radix_sort_scratch_words(uint64_t n);
+cudaError_t launch_radix_sort_pairs(uint32_t *d_keys, uint32_t *d_vals, uint64_t n, int key_bits, uint32_t *d_scratch,
+                                    cudaStream_t st);
 // With d_n, the survivor count is read on the device from *d_n (n_ids bounds it; a larger count means 0).
 cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
                                uint64_t n_ids, SeqView ref, SeqView qry, const ScoreArgs &sa,
                                hspz_segment_pair *d_out, uint8_t *d_done, cudaStream_t st,
-                               const uint64_t *d_n = nullptr);
+                               const uint64_t *d_n = nullptr, bool grouped = false);
 // stable compaction in three launches; d_scratch holds compact_scratch_words(n) uint32.
 // With d_n, the flag count is read on the device from *d_n (n bounds it; a larger count means 0).
 uint64_t compact_scratch_words(uint64_t n);

@@ -224,7 +224,8 @@ __global__ void __launch_bounds__(256, HSPZ_MAT_MIN_BLOCKS) k_materialize_blocks
                                                             const uint32_t *__restrict__ qry_rev, ScoreArgs sa,
                                                             uint4 *__restrict__ out, uint8_t *__restrict__ done,
                                                             ChainSide *__restrict__ sR, ChainSide *__restrict__ sL,
-                                                            ChainInfo *__restrict__ info) {
+                                                            ChainInfo *__restrict__ info,
+                                                            const uint32_t *__restrict__ out_pos) {
     __shared__ int tab[25];
     if (threadIdx.x < 25) tab[threadIdx.x] = sa.m[threadIdx.x];
     __syncthreads();
@@ -396,8 +397,9 @@ __global__ void __launch_bounds__(256, HSPZ_MAT_MIN_BLOCKS) k_materialize_blocks
                 ok = 1;
             }
         }
-        out[k] = rec;
-        done[k] = ok;
+        const uint64_t ko = out_pos ? (uint64_t)out_pos[k] : k;  // grouped order: back to the list's
+        out[ko] = rec;
+        done[ko] = ok;
     }
 }
 
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(256) k_chain_resolve(const uint2 *__restrict__
                                                        const ChainSide *__restrict__ sR,
                                                        const ChainSide *__restrict__ sL,
                                                        const ChainInfo *__restrict__ info, uint4 *__restrict__ out,
-                                                       uint8_t *__restrict__ done) {
+                                                       uint8_t *__restrict__ done, const uint32_t *__restrict__ out_pos) {
     if (d_n) n_ids = live_count(*d_n, n_off, n_ids, n_total);
     const int lane = threadIdx.x & 31;
     const uint64_t n_seg = (n_ids + kChainSeg - 1) / kChainSeg;
@@ -494,8 +496,9 @@ __global__ void __launch_bounds__(256) k_chain_resolve(const uint2 *__restrict__
             rec = make_uint4(a.x - nL, a.y - nL, nL + nR - 1u, (uint32_t)(int32_t)score);
             ok = 1;
         }
-        out[j] = rec;
-        done[j] = ok;
+        const uint64_t jo = out_pos ? (uint64_t)out_pos[j] : j;
+        out[jo] = rec;
+        done[jo] = ok;
     }
 }
 
@@ -532,12 +535,30 @@ __global__ void __launch_bounds__(128) k_materialize(const uint2 *__restrict__ a
     }
 }
 
+// Grouped order: key = the diagonal (ref end - query end) of entry j's anchor,
+// all ones for an entry outside the sequences; value = j.
+__global__ void k_diag_keys(const uint2 *__restrict__ anchors, uint64_t n_anchors, uint32_t id_base,
+                            const uint32_t *__restrict__ ids, uint64_t n, uint64_t Lr, uint64_t Lq,
+                            uint32_t *__restrict__ keys, uint32_t *__restrict__ vals) {
+    for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n; j += (uint64_t)gridDim.x * blockDim.x) {
+        const uint2 a = survivor_anchor(anchors, n_anchors, id_base, ids, j);
+        keys[j] = (a.x < Lr && a.y < Lq) ? a.x - a.y : 0xFFFFFFFFu;
+        vals[j] = (uint32_t)j;
+    }
+}
+
+__global__ void k_gather_ids(const uint32_t *__restrict__ ids, const uint32_t *__restrict__ perm, uint64_t n,
+                             uint32_t *__restrict__ out) {
+    for (uint64_t j = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; j < n; j += (uint64_t)gridDim.x * blockDim.x)
+        out[j] = ids[perm[j]];
+}
+
 }  // namespace
 
 cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
                                uint64_t n_ids,
                                SeqView ref, SeqView qry, const ScoreArgs &sa, hspz_segment_pair *d_out,
-                               uint8_t *d_done, cudaStream_t st, const uint64_t *d_n) {
+                               uint8_t *d_done, cudaStream_t st, const uint64_t *d_n, bool grouped) {
     if (!n_ids) return cudaSuccess;
     const uint2 *an = reinterpret_cast<const uint2 *>(d_anchors);
     uint4 *out = reinterpret_cast<uint4 *>(d_out);
@@ -548,22 +569,40 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
         if (sa.exact && kMaterializeChain) {
             // walks join their diagonal neighbours' walks and the joins are settled after;
             // slices of at most kChainSlice ids bound the scratch (no link crosses a slice)
+            // grouped (host-known count only): each slice's entries are first sorted by
+            // diagonal (stable, so each diagonal keeps the list's order), walked in that
+            // order, and every record goes back to its entry's place
+            grouped = grouped && !d_n;
             const uint64_t slice = n_ids < kChainSlice ? n_ids : kChainSlice;
+            const uint64_t gwords = grouped ? 3 * slice + radix_sort_scratch_words(slice) : 0;
             void *scratch = nullptr;
-            cudaError_t e = pool_alloc(&scratch, slice * (2 * sizeof(ChainSide) + sizeof(ChainInfo)), st);
+            cudaError_t e = pool_alloc(&scratch, slice * (2 * sizeof(ChainSide) + sizeof(ChainInfo)) + gwords * 4, st);
             if (e != cudaSuccess) return e;
             ChainSide *sR = reinterpret_cast<ChainSide *>(scratch), *sL = sR + slice;
             ChainInfo *info = reinterpret_cast<ChainInfo *>(sL + slice);
+            uint32_t *keys = reinterpret_cast<uint32_t *>(info + slice), *perm = keys + slice, *ids2 = perm + slice,
+                     *rscratch = ids2 + slice;
             auto kern = has_n ? k_materialize_blocks<true, true> : k_materialize_blocks<false, true>;
             const uint64_t segs = (slice + kChainSeg - 1) / kChainSeg, sb = (segs + 7) / 8;  // a warp per segment
             const unsigned gs = (unsigned)((slice + 255) / 256 < 152ull * 64 ? (slice + 255) / 256 : 152ull * 64);
             const unsigned gr = (unsigned)(sb < 152ull * 64 ? sb : 152ull * 64);
             for (uint64_t off = 0; off < n_ids && e == cudaSuccess; off += slice) {
                 const uint64_t len = n_ids - off < slice ? n_ids - off : slice;
-                kern<<<gs, 256, 0, st>>>(an, n_anchors, id_base, d_ids + off, len, d_n, off, n_ids, seqs(ref, qry), ref.rev,
-                                         qry.rev, sa, out + off, d_done + off, sR, sL, info); count_launch();
-                k_chain_resolve<<<gr, 256, 0, st>>>(an, n_anchors, id_base, d_ids + off, len, d_n, off, n_ids, sa.T, sR, sL,
-                                                    info, out + off, d_done + off); count_launch();
+                const uint32_t *ids = d_ids + off, *pos = nullptr;
+                if (grouped) {
+                    k_diag_keys<<<grid_cap(len, 256), 256, 0, st>>>(an, n_anchors, id_base, ids, len, ref.len, qry.len,
+                                                                    keys, perm); count_launch();
+                    e = cudaGetLastError();
+                    if (e == cudaSuccess) e = launch_radix_sort_pairs(keys, perm, len, 32, rscratch, st);
+                    if (e != cudaSuccess) break;
+                    k_gather_ids<<<grid_cap(len, 256), 256, 0, st>>>(ids, perm, len, ids2); count_launch();
+                    ids = ids2;
+                    pos = perm;
+                }
+                kern<<<gs, 256, 0, st>>>(an, n_anchors, id_base, ids, len, d_n, off, n_ids, seqs(ref, qry), ref.rev,
+                                         qry.rev, sa, out + off, d_done + off, sR, sL, info, pos); count_launch();
+                k_chain_resolve<<<gr, 256, 0, st>>>(an, n_anchors, id_base, ids, len, d_n, off, n_ids, sa.T, sR, sL,
+                                                    info, out + off, d_done + off, pos); count_launch();
                 e = cudaGetLastError();
             }
             const cudaError_t ef = pool_free(scratch, st);
@@ -572,7 +611,7 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
         if (sa.exact) {
             auto kern = has_n ? k_materialize_blocks<true, false> : k_materialize_blocks<false, false>;
             kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, 0, n_ids, seqs(ref, qry), ref.rev, qry.rev,
-                                    sa, out, d_done, nullptr, nullptr, nullptr); count_launch();
+                                    sa, out, d_done, nullptr, nullptr, nullptr, nullptr); count_launch();
         } else {
             auto kern = has_n ? k_materialize_lane<true> : k_materialize_lane<false>;
             kern<<<g, 256, 0, st>>>(an, n_anchors, id_base, d_ids, n_ids, d_n, seqs(ref, qry), ref.rev, qry.rev, sa,

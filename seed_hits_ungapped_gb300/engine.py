@@ -62,7 +62,8 @@ def _np_u32(t):
 class HspEngine:
     """Reference index + scoring parameters + device buffers for repeated batches."""
 
-    def __init__(self, ref, matrix, xdrop: int, K: int, pattern: str = hspz.DEFAULT_PATTERN, stream=None):
+    def __init__(self, ref, matrix, xdrop: int, K: int, pattern: str = hspz.DEFAULT_PATTERN, stream=None,
+                 group: bool = False):
         import torch
         self.torch = torch
         if not torch.cuda.is_available():
@@ -70,6 +71,7 @@ class HspEngine:
         d_ref = ref if isinstance(ref, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(ref, np.uint8))
         d_ref = d_ref.to(device="cuda", dtype=torch.uint8).contiguous()
         self.stream = stream
+        self.group = group  # materialize repetitive chunks in diagonal order
         self.index = hspz.hspz_build_index(d_ref, pattern, stream=stream)
         self.ref_len = d_ref.numel()
         self.params = hspz.score_params(matrix, xdrop, K)
@@ -100,6 +102,30 @@ class HspEngine:
                 raise
             ids = self.buffer(name, e.needed, torch.int32)
             return ids, hspz.hspz_compact(flags, n, id_base, ids, stream=self.stream)
+
+    def _process_chunk_grouped(self, plan, c: int, n: int, anchors, flags, bufset: str, time_gate: bool = False):
+        """A repetitive chunk step by step: fused expansion + gate, compaction,
+        materialization in diagonal order, accepted compaction (two host
+        synchronizations instead of one).  time_gate: the fused launch's
+        duration from events on the engine's stream."""
+        torch = self.torch
+        hb = int(plan.chunks[c, 2])
+        ks = self._torch_stream()
+        if time_gate:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(ks)
+        hspz.hspz_expand_gate(plan, c, self.params, anchors, flags, stream=self.stream)
+        if time_gate:
+            e1.record(ks)
+        ids, ns = self._compact(flags, n, hb, "ids" + bufset)
+        rec = self.buffer("records" + bufset, max(ns, 1), torch.int32, 4)
+        done = self.buffer("done" + bufset, max(ns, 1), torch.uint8)
+        if ns:
+            hspz.hspz_materialize(self.index, plan, anchors, hb, ids, ns, self.params, rec, done,
+                                  stream=self.stream, grouped=True)
+        acc = self.buffer("accepted" + bufset, max(ns, 1), torch.int32)
+        na = hspz.hspz_compact(done, ns, 0, acc, stream=self.stream) if ns else 0
+        return n, ns, na, (e0.elapsed_time(e1) if time_gate else None)
 
     def _torch_stream(self):
         torch = self.torch
@@ -151,6 +177,21 @@ class HspEngine:
     def plan(self, d_query, max_hits: int = 0, walk_full: bool = False):
         return hspz.hspz_find_hits(self.index, d_query, max_hits, walk_full, stream=self.stream)
 
+    # with group=True a chunk with at least this many hits per seed is taken as
+    # repetitive: the ids of one seed then lie on many diagonals, and
+    # materialization in diagonal order (hspz_materialize_grouped) lets the
+    # survivors of each diagonal share walks.  It pays when repeats are long
+    # (a 4 kbp poly-A run: the chunking workload's step 35.7 -> 27.6 ms with
+    # every chunk grouped) and costs more than it saves when they are short
+    # ((CA)n runs of 20-200 bp: dense's step 283 -> 506 ms), so it is off by
+    # default.
+    GROUP_HITS_PER_SEED = 64
+
+    def chunk_is_repetitive(self, plan, c: int) -> bool:
+        seeds = int(plan.chunks[c, 1]) - int(plan.chunks[c, 0])
+        hits = int(plan.chunks[c, 3]) - int(plan.chunks[c, 2])
+        return self.group and seeds > 0 and hits >= self.GROUP_HITS_PER_SEED * seeds
+
     def process_chunk(self, plan, c: int, time_gate: bool = False, bufset: str = ""):
         """hspz_process_chunk on the engine's buffers, growing the survivor
         buffers and running the chunk again when they are too small.
@@ -161,6 +202,8 @@ class HspEngine:
         anchors = self.buffer("anchors", n, torch.int32, 2)
         flags = self.buffer("flags", n, torch.uint8)
         ids_name = "ids" + bufset
+        if self.chunk_is_repetitive(plan, c):
+            return self._process_chunk_grouped(plan, c, n, anchors, flags, bufset, time_gate)
         cap = self._bufs[ids_name].shape[0] if ids_name in self._bufs else max(1024, n // 32)
         while True:
             bufs = [self.buffer(ids_name, cap, torch.int32), self.buffer("records" + bufset, cap, torch.int32, 4),

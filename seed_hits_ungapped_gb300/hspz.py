@@ -35,7 +35,7 @@ EXPORTS = [
     "hspz_plan_info", "hspz_plan_chunks", "hspz_plan_prefix", "hspz_expand", "hspz_expand_gate",
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
     "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed", "hspz_process_chunk",
-    "hspz_gather_records", "hspz_dedup", "hspz_release_cached_memory",
+    "hspz_gather_records", "hspz_dedup", "hspz_release_cached_memory", "hspz_materialize_grouped",
 ]
 
 
@@ -90,6 +90,7 @@ def load_library():
         "hspz_score_gate": (ctypes.c_int, [VP, VP, VP, U64, P(hspz_score_params), VP, VP]),
         "hspz_compact": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
         "hspz_materialize": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
+        "hspz_materialize_grouped": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
         "hspz_chunk_walk_host": (ctypes.c_int, [VP, U64, U64, ctypes.c_int, P(hspz_chunk), U32, P(U32)]),
         "hspz_gather_records": (ctypes.c_int, [VP, VP, U64, VP, VP]),
         "hspz_dedup": (ctypes.c_int, [VP, U64, VP, U64, P(U64), VP]),
@@ -370,15 +371,18 @@ def hspz_compact_noalloc(d_flags, n: int, id_base: int, d_ids, stream=None) -> i
 
 
 def hspz_materialize(index: Index, plan: Plan, d_anchors, id_base: int, d_ids, n_ids: int,
-                     params: hspz_score_params, d_out, d_done, stream=None):
+                     params: hspz_score_params, d_out, d_done, stream=None, grouped: bool = False):
+    """grouped=True calls hspz_materialize_grouped (ids taken in diagonal order)."""
     import torch
     if d_ids.numel() < n_ids or d_out.numel() < 4 * n_ids or d_done.numel() < n_ids:
         raise ValueError("buffers shorter than n_ids")
-    rc = load_library().hspz_materialize(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"),
-                                         d_anchors.numel() // 2, int(id_base), _dptr(d_ids, torch.int32, "d_ids"), int(n_ids),
-                                         ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
-                                         _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
-    _check(rc, "hspz_materialize")
+    lib = load_library()
+    fn = lib.hspz_materialize_grouped if grouped else lib.hspz_materialize
+    rc = fn(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"),
+            d_anchors.numel() // 2, int(id_base), _dptr(d_ids, torch.int32, "d_ids"), int(n_ids),
+            ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
+            _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
+    _check(rc, "hspz_materialize_grouped" if grouped else "hspz_materialize")
 
 
 def hspz_release_cached_memory():

@@ -352,8 +352,9 @@ def test_materialize_any_id_order(torch_cuda):
     """E.1-E.5 per survivor, whatever the id list: ascending survivors (long
     runs of neighbours on one diagonal), reversed, shuffled, with duplicates,
     with ids outside the anchors, every anchor of a chunk, and lists cut so
-    that runs start and end at every place.  Each record must equal the
-    oracle's record for that id alone."""
+    that runs start and end at every place; in list order and in diagonal
+    order (grouped).  Each record must equal the oracle's record for that id
+    alone, at that id's place."""
     from seed_hits_ungapped_gb300 import hspz
     torch = torch_cuda
     rng = np.random.default_rng(23)
@@ -381,16 +382,18 @@ def test_materialize_any_id_order(torch_cuda):
             ids = (np.asarray(ids_local, np.int64) + base).astype(np.uint32)
             k = ids.size
             d_ids = torch.from_numpy(ids.view(np.int32)).cuda()
-            out = torch.full((max(k, 1), 4), -3, dtype=torch.int32, device="cuda")
-            done = torch.full((max(k, 1),), 9, dtype=torch.uint8, device="cuda")
-            hspz.hspz_materialize(eng.index, plan, anchors, base, d_ids, k, eng.params, out, done)
             # an id outside the anchors gets an empty record (the oracle takes valid ids only)
             valid = np.asarray(ids_local, np.int64) < n
             rec_o = np.zeros((k, 4), np.int32)
             done_o = np.zeros(k, np.uint8)
             rec_o[valid], done_o[valid] = oracle.materialize(r, q, a_np, base, ids[valid], m, 910, 3000)
-            assert np.array_equal(done[:k].cpu().numpy(), done_o)
-            assert np.array_equal(out[:k].cpu().numpy(), rec_o)
+            for grouped in (False, True):
+                out = torch.full((max(k, 1), 4), -3, dtype=torch.int32, device="cuda")
+                done = torch.full((max(k, 1),), 9, dtype=torch.uint8, device="cuda")
+                hspz.hspz_materialize(eng.index, plan, anchors, base, d_ids, k, eng.params, out, done,
+                                      grouped=grouped)
+                assert np.array_equal(done[:k].cpu().numpy(), done_o)
+                assert np.array_equal(out[:k].cpu().numpy(), rec_o)
 
 
 def test_run_stream_batches_match_oracle(torch_cuda):
@@ -416,3 +419,34 @@ def test_run_stream_batches_match_oracle(torch_cuda):
                 assert np.array_equal(g.accepted, o["accepted"])
             got += 1
         assert got == len(qs)
+
+
+def test_repetitive_chunks_group_by_diagonal(torch_cuda):
+    """Poly-A and (CA)n repeats: one seed hits many reference positions, so a
+    chunk averages >= 64 hits per seed and an engine with group=True
+    materializes it in diagonal order (hspz_materialize_grouped).  Everything
+    must still equal the oracle, with and without MAX_HITS cuts, and with
+    grouping off."""
+    torch = torch_cuda
+    rng = np.random.default_rng(41)
+    m = synth.hoxd70()
+    ref = rng.integers(0, 4, 30_000).astype(np.uint8)
+    ref[5_000:5_600] = 0                                   # poly-A
+    for i in range(12):                                    # (CA)n copies
+        p0 = 8_000 + 1_500 * i
+        ref[p0:p0 + 160] = np.tile(np.array([1, 0], np.uint8), 80)
+    qry = rng.integers(0, 4, 3_000).astype(np.uint8)
+    qry = np.concatenate([qry[:1_000], np.zeros(500, np.uint8), qry[1_000:2_000],
+                          np.tile(np.array([1, 0], np.uint8), 120), qry[2_000:]])
+    qry[1_200] = 2                                          # a mismatch inside the poly-A run
+    for max_hits, group in ((0, True), (60_000, True), (0, False)):
+        from seed_hits_ungapped_gb300.engine import HspEngine
+        eng = HspEngine(ref, m, 910, 3000, group=group)
+        plan = eng.plan(_dev(torch, qry), max_hits)
+        if group:
+            assert any(eng.chunk_is_repetitive(plan, c) for c in range(plan.n_chunks))
+        plan.close()
+        gpu = eng.run(_dev(torch, qry), max_hits=max_hits, keep=True)
+        orc = oracle.run_path(ref, qry, m, 910, 3000, max_hits=max_hits)
+        assert_same_as_oracle(gpu, orc)
+        assert gpu.n_survivors > 10_000
