@@ -277,12 +277,12 @@ __device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, 
 }
 
 #ifndef HSPZ_GATE_MIN_BLOCKS
-#define HSPZ_GATE_MIN_BLOCKS 5  // resident CTAs per SM the register budget allows
+#define HSPZ_GATE_MIN_BLOCKS 10  // resident CTAs per SM the register budget allows
 #endif
-constexpr int kWWarps = 8;             // warps per CTA
+constexpr int kWWarps = 4;             // warps per CTA
 constexpr int kWUnit = 256;            // anchor slots per warp
 constexpr int kWTile = kWWarps * kWUnit;
-constexpr int kWSeeds = 2048;          // cached seed prefixes per CTA
+constexpr int kWSeeds = 1024;          // cached seed prefixes per CTA
 
 // The seeds of the first and last anchor slot of every tile (thread per tile).
 __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
