@@ -1,0 +1,39 @@
+"""Host-side parts of the benchmark, no GPU: the algorithmic byte count and
+the CPU leg (the oracle's expansion + gate on a bounded sample, and the base
+pairs per anchor that the ALU roofline counts)."""
+import numpy as np
+
+import bench
+import oracle
+from seed_hits_ungapped_gb300 import synth
+
+
+def test_algorithmic_bytes_formula():
+    # 16 B per seed, 13 B per anchor, both sequences once
+    assert bench.algorithmic_bytes(10, 100, 1000, 50) == 16 * 10 + 13 * 100 + 1000 + 50
+    assert bench.algorithmic_bytes(0, 0, 0, 0) == 0
+
+
+def test_cpu_baseline_reports_rate_and_gate_pairs():
+    w = synth.make("tiny", scale=0.2)
+    cpu = bench.run_cpu_baseline(w, seconds=0.5)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
+    ppa = cpu["gate_pairs_per_anchor"]
+    # the sample's pairs per anchor equal the oracle's count over the same anchors
+    idx, pos = oracle.build_index(w.ref)
+    b = oracle.seed_buckets(w.query)
+    P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, b))
+    T = oracle.keep_threshold(w.K)
+    n_seeds = int(cpu["sample"].split("first ")[1].split(" seeds")[0])
+    sub, s0 = [], 0
+    while s0 < n_seeds:
+        s1 = min(n_seeds, s0 + 200_000)
+        hb = int(P[s0 - 1]) if s0 else 0
+        a = oracle.expand(idx, pos, b, P, np.array([s0, s1, hb, P[s1 - 1]], np.uint32))
+        sub.append(a[::16])
+        s0 = s1
+    sub = np.concatenate(sub)
+    want = oracle.gate_pairs(w.ref, w.query, sub, w.matrix, w.xdrop, T) / len(sub)
+    assert abs(ppa - want) < 1e-9
+    # a seed anchor's decision scores at least its left walk through the seed
+    assert ppa > 18
