@@ -184,13 +184,13 @@ __global__ void __launch_bounds__(kFuseThreads) k_expand_gate(const uint32_t *__
 // A round lasts the longest walk of its 32 lanes (for random anchors ~8 steps
 // on the left, ~6 on the right), so these steps are rarely extra, and
 // unrolled steps without votes overlap and address their words with
-// immediate offsets.  Measured on workload_a: (7, 5) and (8, 5) beat shorter
-// and longer leads.
+// immediate offsets.  Measured on workload_a with 4-warp CTAs: (8, 6) beat
+// (8, 5), (7, 6), (7, 5) and shorter leads.
 #ifndef HSPZ_LEAD_LEFT
-#define HSPZ_LEAD_LEFT 7
+#define HSPZ_LEAD_LEFT 8
 #endif
 #ifndef HSPZ_LEAD_RIGHT
-#define HSPZ_LEAD_RIGHT 5
+#define HSPZ_LEAD_RIGHT 6
 #endif
 constexpr int kLeadLeft = HSPZ_LEAD_LEFT, kLeadRight = HSPZ_LEAD_RIGHT;
 
