@@ -466,14 +466,39 @@ def main():
     return 0
 
 
-def kernel_rev() -> str:
-    """Content hash of the sources that define the fused expansion + gate
-    kernel (ties stored ncu counters to a kernel version)."""
+def code_only(src: str) -> str:
+    """C/CUDA source without comments and blank space (string literals kept)."""
+    import re
+    out, i, n = [], 0, len(src)
+    while i < n:
+        if src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif src[i] == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        else:
+            out.append(src[i])
+            i += 1
+    return re.sub(r"\s+", " ", "".join(out)).strip()
+
+
+def kernel_rev(read=None) -> str:
+    """Hash of the code (comments and blank space left out) of the sources
+    that define the fused expansion + gate kernel: ties stored ncu counters
+    to a kernel version.  `read(name)` may supply a file's text."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "seed_hits_ungapped_gb300", "csrc")
     for f in ("hspz_gate.cu", "hspz_walk.cuh", "hspz_internal.cuh"):
-        h.update(open(os.path.join(d, f), "rb").read())
+        text = read(f) if read else open(os.path.join(d, f)).read()
+        h.update(code_only(text).encode())
     return h.hexdigest()[:16]
 
 

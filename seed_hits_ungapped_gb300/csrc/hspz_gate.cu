@@ -301,11 +301,12 @@ __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32
 // every warp works alone on its own 256 slots:
 //   1. lane l expands slots 8l..8l+7 of the warp's share into shared memory
 //      (search for the first slot's seed, then walk forward);
-//   2. the gate runs in 8 synchronous rounds of 32 anchors (one per lane):
-//      all lanes start their left side together, step until every lane has
-//      flagged a step that may hold its stop, reaches `need` or ends at the
-//      edge, settle together, then the same for the right side;
-//   3. the warp stores its anchors and flags with coalesced writes.
+//   2. the gate runs in 8 synchronous rounds of 32 anchors (one per lane,
+//      gate_round): all lanes walk their left sides together, first a fixed
+//      number of branch-free steps, then single steps under a warp vote
+//      while any lane still walks; then their right sides the same way;
+//   3. the warp stores its flags (per round) and anchors with coalesced,
+//      cache-streaming writes.
 template <bool HAS_N, bool EXACT>
 __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     k_expand_gate_w(const uint32_t *__restrict__ P, const uint32_t *__restrict__ lo,
