@@ -37,3 +37,10 @@ def test_cpu_baseline_reports_rate_and_gate_pairs():
     assert abs(ppa - want) < 1e-9
     # a seed anchor's decision scores at least its left walk through the seed
     assert ppa > 18
+
+
+def test_kernel_hash_ignores_comments_only():
+    src = 'int a = 1;  // walk\n/* step\n   block */\nconst char *s = "//x /*y*/";\nint b = a + 1;\n'
+    assert bench.code_only(src) == 'int a = 1; const char *s = "//x /*y*/"; int b = a + 1;'
+    assert bench.code_only(src.replace("// walk", "// other words")) == bench.code_only(src)
+    assert bench.code_only(src.replace("a + 1", "a + 2")) != bench.code_only(src)
