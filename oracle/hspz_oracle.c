@@ -20,7 +20,11 @@
  * Hit discovery", brute-force seed matching, closed forms for all-match
  * segments, the maximum-prefix-sum brute force at infinite X-drop, hand cases
  * for the drop boundary and the earliest-maximum tie rule, an exhaustive f32
- * check of the keep threshold, and the exact 2^32 refusal edge.
+ * check of the keep threshold, and the exact 2^32 refusal edge.  The gate
+ * flags are pinned by hand totals at exactly T and T - 1, by the best window
+ * through each anchor at infinite X-drop (kept and rejected anchors), and by
+ * a prefix-sum formulation of the X-drop stop at finite X; the rejected slot
+ * of the materializer by a hand case below T.
  */
 #include <stdint.h>
 #include <stdlib.h>

@@ -469,3 +469,107 @@ def test_gate_pairs_closed_forms():
     # left walk has 4 pairs (400), the right needs 6 more
     assert oracle.gate_pairs(s, s, np.array([[4, 4]], np.uint32), m, 910, 1000) == 4 + 6
     assert oracle.gate_pairs(s, s, np.zeros((0, 2), np.uint32), m, 910, 1000) == 0
+
+
+# ---------------------------------------------------------------- gate flags (D.2/D.3: flag = total >= T)
+
+def _hand_gate_case():
+    """Anchor at 5 of a 10-base pair of sequences under the hand matrix.
+
+    Left side (bases 4, 3, 2, 1, 0, outward): ref C/query A +40, then A/C
+    -10, A/A +10, A/A +10, A/C -10: running sums 40, 30, 40, 50, 40, so the
+    left maximum is 50 (4 bases).  Right side (bases 5..9): A/A +10, A/C -10,
+    A/C -10, G/G +50, T/A -100: sums 10, 0, -10, 40, -60, so the right
+    maximum is 40 with X = 20 (deficit exactly X is not a stop) and 10 with
+    X = 19 (the walk stops at the third base).  Totals: 90 and 60.
+    """
+    ref = _seq("AAAAC" + "AAAGT")
+    qry = _seq("CAACA" + "ACCGA")
+    return ref, qry, np.array([[5, 5]], np.uint32)
+
+
+def test_gate_flag_at_exactly_T_and_T_minus_1():
+    m = _hand_matrix()
+    ref, qry, a = _hand_gate_case()
+    sc = oracle.side_scores(ref, qry, a, m, 20)[0]
+    assert sc.tolist() == [50, 4, 40, 4]
+    assert oracle.gate(ref, qry, a, m, 20, 90).tolist() == [1]
+    assert oracle.gate(ref, qry, a, m, 20, 91).tolist() == [0]
+    # X = 19 stops the right walk before its +50 base: total 60
+    assert oracle.gate(ref, qry, a, m, 19, 60).tolist() == [1]
+    assert oracle.gate(ref, qry, a, m, 19, 61).tolist() == [0]
+    assert oracle.gate(ref, qry, a, m, 19, 90).tolist() == [0]
+
+
+def test_gate_rejected_slot_of_materialize_is_zero():
+    m = _hand_matrix()
+    ref, qry, a = _hand_gate_case()
+    rec, done = oracle.materialize(ref, qry, a, 0, [0], m, 20, 91)
+    assert rec[0].tolist() == [0, 0, 0, 0] and done[0] == 0
+    # at T = total the same id is accepted: left extent 4, right extent 4 bases
+    rec, done = oracle.materialize(ref, qry, a, 0, [0], m, 20, 90)
+    assert rec[0].tolist() == [1, 1, 7, 90] and done[0] == 1
+    # ids are global: with id_base 7, id 7 addresses the same anchor 0
+    rec, done = oracle.materialize(ref, qry, a, 7, [7], m, 20, 91)
+    assert rec[0].tolist() == [0, 0, 0, 0] and done[0] == 0
+
+
+def _random_gate_case(seed, L=90, n_anchor=60):
+    rng = np.random.default_rng(seed)
+    ref = rng.integers(0, 5, L).astype(np.uint8)
+    qry = np.where(rng.random(L) < 0.55, ref, rng.integers(0, 5, L)).astype(np.uint8)
+    m = rng.integers(-60, 61, (5, 5)).astype(np.int32)  # asymmetric
+    anchors = np.stack([rng.integers(0, L, n_anchor), rng.integers(0, L, n_anchor)], 1).astype(np.uint32)
+    anchors[: n_anchor // 3, 1] = anchors[: n_anchor // 3, 0]  # some on the main diagonal (long walks)
+    return ref, qry, m, anchors
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_gate_at_infinite_x_is_best_window_through_the_anchor(seed):
+    """X = infinity: the walk never stops before an edge, so the total is the
+    best score of any window [a-l, a+r) around the anchor (the empty window
+    scores 0), found here by enumerating every (l, r)."""
+    ref, qry, m, anchors = _random_gate_case(seed)
+    best = []
+    for ar, aq in anchors.astype(np.int64):
+        b = 0
+        for l in range(min(ar, aq) + 1):
+            for r in range(min(ref.size - ar, qry.size - aq) + 1):
+                s = sum(int(m[ref[ar + k], qry[aq + k]]) for k in range(-l, r))
+                b = max(b, s)
+        best.append(b)
+    best = np.array(best)
+    assert best.min() < np.median(best) < best.max()
+    for T in (int(np.median(best)), int(np.median(best)) + 1, int(best.max()), int(best.max()) + 1, 1):
+        flags = oracle.gate(ref, qry, anchors, m, 1 << 30, T)
+        assert flags.tolist() == (best >= T).astype(np.uint8).tolist()
+    assert 0 < oracle.gate(ref, qry, anchors, m, 1 << 30, int(np.median(best))).sum() < len(anchors)
+
+
+def _side_max_np(m, ref, qry, ar, aq, right, X):
+    """The X-drop side maximum from prefix sums: n* = the first step whose
+    sum falls more than X below the maximum of the sums before it (the
+    empty prefix included); the result is the largest sum before n*."""
+    if right:
+        k = min(ref.size - ar, qry.size - aq)
+        sc = m[ref[ar:ar + k], qry[aq:aq + k]].astype(np.int64)
+    else:
+        k = min(ar, aq)
+        sc = m[ref[ar - k:ar][::-1], qry[aq - k:aq][::-1]].astype(np.int64)
+    S = np.concatenate([[0], np.cumsum(sc)])
+    before = np.maximum.accumulate(S)[:-1]
+    drop = np.flatnonzero(before - S[1:] > X)
+    stop = drop[0] + 1 if drop.size else S.size
+    return int(S[:stop].max())
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("X", [0, 45, 130])
+def test_gate_flags_match_prefix_sum_form(seed, X):
+    ref, qry, m, anchors = _random_gate_case(100 + seed, L=200, n_anchor=150)
+    tot = np.array([_side_max_np(m, ref, qry, ar, aq, False, X) + _side_max_np(m, ref, qry, ar, aq, True, X)
+                    for ar, aq in anchors.astype(np.int64)])
+    for T in sorted({1, int(np.median(tot)), int(np.median(tot)) + 1, int(tot.max()), int(tot.max()) + 1}):
+        T = max(T, 1)
+        flags = oracle.gate(ref, qry, anchors, m, X, T)
+        assert flags.tolist() == (tot >= T).astype(np.uint8).tolist()
