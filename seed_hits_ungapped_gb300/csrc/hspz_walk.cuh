@@ -219,12 +219,25 @@ __device__ __forceinline__ bool walk_resolve(WalkState &w, const int (&Sv)[8], i
     return false;
 }
 
+// hi = max(M, the eight sums of a step), lo = the lowest of the eight.
+__device__ __forceinline__ void step_range(const int (&Sv)[8], int M, int &hi, int &lo) {
+    hi = max(max(max(Sv[0], Sv[1]), max(Sv[2], Sv[3])), max(max(Sv[4], Sv[5]), max(Sv[6], Sv[7])));
+    hi = max(hi, M);
+    lo = min(min(min(Sv[0], Sv[1]), min(Sv[2], Sv[3])), min(min(Sv[4], Sv[5]), min(Sv[6], Sv[7])));
+}
+
 // The 8-base step with an exact stop test, for scoring where X >= 7 * the
 // largest single-pair score (and X >= 0).  Base k of the step stops the walk
 // when it falls more than X below the running maximum m(k-1) of the bases
 // before it.  After such a stop the remaining (at most 7) sums of the step
 // cannot climb back above m(k-1), so the step's final running maximum is the
 // side maximum at the stop: the step never has to be replayed base by base.
+// Nor does the stop test need the running maxima: with hi = max(M, sums of
+// the step) and lo = the lowest sum of the step, some base stops the walk
+// exactly when lo + X < hi.  (A stop at k gives lo <= S(k) < m(k-1) - X <=
+// hi - X.  Conversely, if lo + X < hi and hi is M or a sum before lo's base,
+// lo's base itself stops the walk; hi cannot come after lo's base, since
+// at most 7 pairs lie between them and they cannot rise by more than X.)
 // The step has no branches or selects, so every lane of a round runs it
 // together.  A lane whose side is over (stop, `need` reached or edge) gets
 // rem = 0: its keep mask is then empty, so its later steps score nothing and
@@ -239,14 +252,10 @@ __device__ __forceinline__ void walk_step_lead(WalkState &w, uint32_t tlo, uint3
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
     int Sv[8];
     step_sums<!BACK, HAS_N>(R, Q, step_keep<BACK>(w.rem), tlo, thi, tab25, w.S, Sv);
-    int m = w.M, d = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        d |= Sv[k] + X - m;
-        m = max(m, Sv[k]);
-    }
-    const bool over = ((d | (need - 1 - m)) < 0) | (w.rem <= 8);
-    w.M = m;
+    int hi, lo;
+    step_range(Sv, w.M, hi, lo);
+    const bool over = (((lo + X - hi) | (need - 1 - hi)) < 0) | (w.rem <= 8);
+    w.M = hi;
     w.S = Sv[7];
     w.rem = over ? 0u : w.rem - 8u;
     if (BACK) {
@@ -281,15 +290,11 @@ __device__ __forceinline__ void walk_step_inner(WalkState &w, uint32_t &keep, ui
     const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
     int Sv[8];
     step_sums<!BACK, HAS_N>(R, Q, keep, tlo, thi, tab25, w.S, Sv);
-    int m = w.M, d = 0;
-#pragma unroll
-    for (int k = 0; k < 8; k++) {
-        d |= Sv[k] + X - m;
-        m = max(m, Sv[k]);
-    }
-    w.M = m;
+    int hi, lo;
+    step_range(Sv, w.M, hi, lo);
+    w.M = hi;
     w.S = Sv[7];
-    keep = ((d | (need - 1 - m)) < 0) ? 0u : keep;
+    keep = (((lo + X - hi) | (need - 1 - hi)) < 0) ? 0u : keep;
     if (BACK) {
         w.r1 = w.r0;
         w.q1 = w.q0;
