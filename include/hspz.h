@@ -248,12 +248,17 @@ int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t 
  * cause.  Same arguments, result and statuses as hspz_compact, for at most
  * hspz_compact_noalloc_max_flags() = 2^28 flags (larger n: HSPZ_E_INVAL with
  * a message in hspz_last_error).  Its scratch is one fixed device array of
- * about 768 KiB inside the library, held by every GPU that loads the library
- * until the process exits.  The first call on a device looks up that array's
- * device address (once per device, with the device current); make that first
- * call before any stream capture.  All calls share the one array, so calls
- * that overlap on the GPU (different streams or threads at the same time)
- * race and must be serialized by the caller.  Synchronizes `stream`.
+ * about 768 KiB inside the library.  CUDA loads library code lazily, so that
+ * array and the compaction kernels take their device memory on a device only
+ * when this call first runs there (even with n = 0: that call loads them and
+ * does nothing else); from then on they stay until the process exits.  Make
+ * one call per device, n = 0 will do, before handing the device's memory to
+ * another allocator, and before any stream capture.  Every call looks up the
+ * array's device address for the current device, so a cudaDeviceReset does
+ * not leave a stale address (the next call loads the code again).  All calls
+ * share the one array, so calls that overlap on the GPU (different streams or
+ * threads at the same time) race and must be serialized by the caller.
+ * Synchronizes `stream` (except with n = 0).
  * ------------------------------------------------------------------------ */
 int hspz_compact_noalloc(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
                          uint64_t *n_out, void *stream);

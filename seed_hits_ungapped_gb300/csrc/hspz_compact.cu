@@ -127,6 +127,16 @@ __global__ void __launch_bounds__(kThreads) k_emit(const uint8_t *__restrict__ f
 
 }  // namespace
 
+cudaError_t preload_compact_kernels() {
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, k_count_flags<true>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_count_flags<false>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_scan_counts);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_emit<true>);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, k_emit<false>);
+    return e;
+}
+
 uint64_t compact_scratch_words(uint64_t n) {
     const uint64_t nb = (n + kTile - 1) / kTile;
     return nb + 2 * nb + 2;  // counts (u32) + exclusive offsets (u64)

@@ -111,6 +111,9 @@ cudaError_t launch_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors,
 // stable compaction in three launches; d_scratch holds compact_scratch_words(n) uint32.
 // With d_n, the flag count is read on the device from *d_n (n bounds it; a larger count means 0).
 uint64_t compact_scratch_words(uint64_t n);
+// Loads the compaction kernels onto the current device now (under lazy module
+// loading a kernel is otherwise loaded, taking device memory, at its first launch).
+cudaError_t preload_compact_kernels();
 cudaError_t launch_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t *d_ids, uint64_t cap,
                            uint32_t *d_scratch, uint64_t *d_total, cudaStream_t st, const uint64_t *d_n = nullptr);
 

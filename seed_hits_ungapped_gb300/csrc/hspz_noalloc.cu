@@ -6,10 +6,16 @@
 // (so any cudaMalloc fails), or one that must not pay the implicit device
 // synchronization that cudaMalloc/cudaFree can cause in a latency-bound loop.
 // This entry point serves them: it calls no cudaMalloc, cudaFree or other
-// allocating routine.  The scratch is a file-scope __device__ array that every
-// GPU loading the library holds until the process exits.
-#include <mutex>
-
+// allocating routine.  The scratch is a file-scope __device__ array.
+//
+// CUDA loads modules lazily by default, so the array (and the compaction
+// kernels) would otherwise take their device memory at the first call that
+// launches work, possibly after the caller has given all memory away.  Every
+// call therefore first makes sure, for the current device, that the kernels
+// are loaded and the array exists (the first call on a device loads them,
+// even with n = 0), then looks up the array's device address.  The lookup is
+// repeated on every call so the address always belongs to the device's
+// current context (a cudaDeviceReset drops the old one).
 #include "hspz_internal.cuh"
 
 namespace hspz {
@@ -22,28 +28,16 @@ constexpr uint64_t kNoAllocWords = 3 * (kNoAllocMaxFlags / 4096) + 8;
 
 static __device__ __align__(256) uint32_t g_noalloc_scratch[kNoAllocWords];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-uint32_t *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once
-// per device; host code only ever sees a host-side stand-in for the symbol).
-int scratch_address(uint32_t **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "hspz_compact_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) {
-        set_error("hspz_compact_noalloc: device ordinal out of range");
-        return HSPZ_E_UNSUPPORTED;
-    }
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "hspz_compact_noalloc: cudaGetSymbolAddress");
-        g_scratch_ptr[dev] = static_cast<uint32_t *>(p);
-    }
-    *out = g_scratch_ptr[dev];
+// Set-up on the current device: load the compaction kernels, then take the
+// scratch array's device address (host code only ever sees a host-side
+// stand-in for the symbol, never a device address).
+int setup_scratch(uint32_t **out) {
+    cudaError_t e = preload_compact_kernels();
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_compact_noalloc: loading the compaction kernels");
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "hspz_compact_noalloc: cudaGetSymbolAddress");
+    *out = static_cast<uint32_t *>(p);
     return HSPZ_OK;
 }
 
@@ -63,10 +57,10 @@ extern "C" int hspz_compact_noalloc(const uint8_t *d_flags, uint64_t n, uint32_t
         return HSPZ_E_INVAL;
     }
     *n_out = 0;
-    if (!n) return HSPZ_OK;
     uint32_t *scratch = nullptr;
-    int rc = scratch_address(&scratch);
+    int rc = setup_scratch(&scratch);
     if (rc) return rc;
+    if (!n) return HSPZ_OK;
     cudaStream_t st = (cudaStream_t)stream;
     // counts and offsets are rewritten in full by every call; the total sits
     // after the largest layout launch_compact can use
