@@ -3,13 +3,15 @@
 One step = the whole path over one synthetic query batch: hit discovery
 (count, prefix, chunk walk), fused expansion + score gate, stable compaction,
 materialization and the accepted compaction.  The metric is anchors per
-second.  The dominant kernel (fused expansion + gate) is bound by integer
-arithmetic: "roofline" reports it against the SMs' int32 rate, counting 4
-operations per base pair the gate decision scores (pairs per anchor measured
-by the oracle on the CPU sample).  It is also reported against the HBM copy
-rate ("hbm_roofline"; "roofline" itself when the CPU sample is skipped) and,
-from ncu instruction counts of the same kernel version, against the SMs'
-instruction issue rate ("issue_roofline").
+second.  "roofline" reports the dominant kernel (fused expansion + gate)
+against the measured HBM copy bandwidth: algorithmic bytes (16 per seed, 13
+per anchor, both sequences once) per launch over the launch's CUDA-event
+time.  That kernel is bound by integer work, not by HBM, so two models are
+reported beside it: "alu_model" (4 int32 operations per base pair the gate
+decision scores, pairs per anchor measured by the oracle on the CPU sample,
+against 128 int32 lanes per SM per cycle) and, from ncu instruction counts
+of the same kernel version, "issue_roofline" (issued lane-instructions
+against the SMs' issue rate).
 Duplicate removal over each batch's accepted HSPs ("dedup") is timed apart
 from the step (--no-dedup skips it).
 
@@ -83,14 +85,16 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, path: str | None = None):
+        import tempfile
         self.gpu = gpu_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_rank%d.csv" % gpu_index)
+        self.path = path or os.path.join(tempfile.gettempdir(), "hspz_bench_clocks_%d_gpu%d.csv"
+                                         % (os.getpid(), gpu_index))
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -126,6 +130,26 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def host_info():
+    """Host cores (nproc) and CPU model of the machine the CPU figures come from.
+    Arm cores name no model in /proc/cpuinfo; their implementer and part
+    numbers stand in for it."""
+    import platform
+    fields = {}
+    try:
+        for line in open("/proc/cpuinfo"):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    model = fields.get("model name")
+    if not model and "cpu part" in fields:
+        model = "%s, cpu implementer %s, cpu part %s" % (platform.machine(), fields.get("cpu implementer", "?"),
+                                                         fields["cpu part"])
+    return {"nproc": os.cpu_count(), "cpu_model": model or platform.machine(), "machine": platform.machine()}
+
+
 def run_cpu_baseline(w, seconds: float = 12.0):
     """The oracle as it stands, single-threaded, on a bounded sample of the
     same workload: expansion + gate over the seeds of the query's leading
@@ -154,7 +178,7 @@ def run_cpu_baseline(w, seconds: float = 12.0):
         s_begin = s_end
     return {"value": done_anchors / t_used, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": "expansion + gate of the first %d seeds (%d anchors) of the %s query, single-threaded C"
-                      % (s_begin, done_anchors, w.name), "seconds": round(t_used, 3),
+                      % (s_begin, done_anchors, w.name), "seconds": round(t_used, 3), "host": host_info(),
             "gate_pairs_per_anchor": pairs / pair_anchors if pair_anchors else None,
             "gate_pairs_sample": "oracle.gate_pairs over every 16th of those anchors (%d)" % pair_anchors}
 
@@ -195,7 +219,7 @@ def reference_arm(args):
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": "per step: expansion + gate + compaction + materialization of %d "
                                        "consecutive seeds of the %s query (single-threaded C oracle)"
-                                       % (sample_seeds, w.name)},
+                                       % (sample_seeds, w.name), "host": host_info()},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -215,6 +239,8 @@ def main():
                     help="size factor of the workload (profiling on smaller cases; 1 = the workload as named)")
     ap.add_argument("--gate", default="fused", choices=["fused", "bucketed"],
                     help="fused expansion + gate (default), or expansion then the reference-bucketed gate (D.5)")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where to write the nvidia-smi clock samples (default: a file in the temp directory)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -276,7 +302,7 @@ def main():
                     ids, n_surv = eng._compact(flags, n, hb, "ids")
                     rec = eng.buffer("records", n_surv, torch.int32, 4)
                     done = eng.buffer("done", n_surv, torch.uint8)
-                    hspz.hspz_materialize(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
+                    hspz.hspz_materialize_plan(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
                     eng._compact(done, n_surv, 0, "accepted")
                 n_anchors += n
             plan.close()
@@ -290,7 +316,7 @@ def main():
     # stream, with an L2 flush between steps outside the events
     step_ms = []
     launches0 = lib.hspz_kernel_launches()
-    with ClockSampler(local) as clocks:
+    with ClockSampler(local, args.clocks_csv) as clocks:
         barrier()
         t_wall0 = time.perf_counter()
         for _ in range(args.steps):
@@ -420,10 +446,12 @@ def main():
            "traffic": traffic, "peak_kind": peak_kind, "kernel": kernel_name,
            "kernel_ms_per_launch": sum(gate_ms) / n_launch,
            "algorithmic_bytes_per_launch": alg_bytes_per_launch}
-    # the bound that holds: integer arithmetic.  Algorithmic work = the base
-    # pairs the gate decision scores (per anchor, from the oracle on the CPU
-    # sample) x 4 integer operations per pair (pair score, running sum,
-    # running maximum, drop test), against 128 int32 lanes per SM per cycle.
+    # a model of the integer work beside the HBM roofline: the base pairs the
+    # gate decision scores (per anchor, from the oracle on the CPU sample) x 4
+    # integer operations per pair (pair score, running sum, running maximum,
+    # drop test), against 128 int32 lanes per SM per cycle.  The step's
+    # PRMT, IDP4A and LOP3 run at 64 lanes per SM per cycle on sm_103a, so
+    # this peak is the IADD/IMNMX rate, an upper bound, not the kernel's.
     alu = None
     if cpu and cpu.get("gate_pairs_per_anchor"):
         sms = torch.cuda.get_device_properties(local).multi_processor_count
@@ -433,8 +461,9 @@ def main():
         t_launch = sum(gate_ms) / n_launch / 1e3
         a_ops = 4 * pairs_launch / t_launch / 1e12
         p_ops = sms * 128 * sm_mhz * 1e6 / 1e12
-        alu = {"bound": "alu", "achieved": a_ops, "peak": p_ops, "unit": "T int32 ops/s", "frac": a_ops / p_ops,
-               "traffic": traffic, "peak_kind": "derived: %d SMs x 128 int32 lanes x %.0f MHz" % (sms, sm_mhz),
+        alu = {"model": "4 int32 operations per base pair the gate decision scores",
+               "achieved": a_ops, "peak": p_ops, "unit": "T int32 ops/s", "frac": a_ops / p_ops,
+               "peak_kind": "derived: %d SMs x 128 int32 lanes (IADD/IMNMX rate) x %.0f MHz" % (sms, sm_mhz),
                "kernel": kernel_name, "kernel_ms_per_launch": sum(gate_ms) / n_launch,
                "ops_per_pair": 4, "gate_pairs_per_anchor": ppa, "gate_pairs_per_launch": pairs_launch,
                "pairs_basis": cpu.get("gate_pairs_sample")}
@@ -452,8 +481,8 @@ def main():
                    "chunks": n_chunks_step, "l2": "flushed (512 MiB write) between timed steps",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "expand_gate_anchors_per_s": n_anchors * args.steps / (sum(gate_ms) / 1e3),
-        "roofline": alu if alu else hbm,
-        "hbm_roofline": hbm if alu else None,
+        "roofline": hbm,
+        "alu_model": alu,
         "issue_roofline": issue,
         "dedup": dedup,
         "cpu_baseline": cpu,

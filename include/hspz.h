@@ -177,7 +177,7 @@ int hspz_expand(const hspz_plan *plan, uint32_t chunk, int mode, hspz_anchor *d_
 
 /* ------------------------------------------------------------------------ *
  * Fused expansion + score gate of one chunk (C.5 + D.1-D.3): writes the same
- * anchors as hspz_expand and, for each, the flag byte of hspz_score_gate.
+ * anchors as hspz_expand and, for each, the flag byte of hspz_score_gate_plan.
  * Uses a small tile table owned by the plan, so two hspz_expand_gate calls on
  * one plan must not run at the same time on the GPU.
  * ------------------------------------------------------------------------ */
@@ -188,7 +188,7 @@ int hspz_expand_gate(const hspz_plan *plan, uint32_t chunk, const hspz_score_par
  * One chunk through the rest of the path with a single host synchronization:
  * the fused expansion + gate (hspz_expand_gate), the stable compaction of the
  * flags into survivor ids (hspz_compact), their materialization
- * (hspz_materialize) and the stable compaction of the done flags into
+ * (hspz_materialize_plan) and the stable compaction of the done flags into
  * accepted indices (positions in the survivor list).  The survivor count
  * stays on the device between the steps.  d_anchors and d_flags need room
  * for the chunk's hits (cap_anchors); d_ids, d_records (16-byte aligned),
@@ -205,21 +205,33 @@ int hspz_process_chunk(const hspz_plan *plan, uint32_t chunk, const hspz_score_p
                        uint64_t *n_survivors, uint64_t *n_accepted, float *gate_ms, void *stream);
 
 /* ------------------------------------------------------------------------ *
- * Score-only X-drop gate ("D. Score gate", D.2-D.3) over n anchors against the
- * index's reference and the plan's query.  Per anchor (a_r, a_q): the right
- * side scores the anchor base and the bases after it, the left side the bases
- * before it; each side walks with S_0 = M_0 = 0, S_n = S_{n-1} + m[ref][qry],
- * stops before step n when M_{n-1} - S_n > xdrop or at a sequence edge, and
- * yields its maximum M.  flag = (M_left + M_right >= T) with T =
- * hspz_keep_threshold(K): 1 keeps, 0 rejects.  An anchor outside the
- * sequences gets flag 0.
+ * Score-only X-drop gate ("D. Score gate", D.1-D.3: anchors and the encoded
+ * sequences in, one flag byte per anchor out) over n anchors of any origin.
+ * d_anchors: n hspz_anchor (reference end, query end) in device memory;
+ * d_ref / d_query: ref_len / query_len base codes (uint8, A0 C1 G2 T3, any
+ * other value N) in device memory.  Per anchor (a_r, a_q): the right side
+ * scores the anchor base and the bases after it, the left side the bases
+ * before it; each side walks with S_0 = M_0 = 0, S_n = S_{n-1} +
+ * m[ref][qry], stops before step n when M_{n-1} - S_n > xdrop or at a
+ * sequence edge, and yields its maximum M.  d_flags[i] = 1 when M_left +
+ * M_right >= T with T = hspz_keep_threshold(K), else 0; an anchor outside the
+ * sequences gets 0.  The call packs both sequences into stream-ordered scratch
+ * from the library's memory pool (about (ref_len + query_len) / 2 + 1 KiB
+ * bytes, freed in stream order) and does not synchronize `stream`.
+ * hspz_score_gate_plan gates against an index and a plan without packing.
  * ------------------------------------------------------------------------ */
-int hspz_score_gate(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors, uint64_t n,
-                    const hspz_score_params *params, uint8_t *d_flags, void *stream);
+int hspz_score_gate(const hspz_anchor *d_anchors, uint64_t n, const uint8_t *d_ref, uint64_t ref_len,
+                    const uint8_t *d_query, uint64_t query_len, const hspz_score_params *params, uint8_t *d_flags,
+                    void *stream);
+
+/* The same gate against the packed reference of `index` and the packed query
+ * of `plan` (made from that index); nothing is packed or allocated. */
+int hspz_score_gate_plan(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors, uint64_t n,
+                         const hspz_score_params *params, uint8_t *d_flags, void *stream);
 
 /* ------------------------------------------------------------------------ *
  * Reference-bucketed score gate ("D. Score gate", D.5): the same flags as
- * hspz_score_gate, computed after a stable counting sort of the anchors into
+ * hspz_score_gate_plan, computed after a stable counting sort of the anchors into
  * n_buckets reference-address windows (1..32; 0 = auto: enough windows that
  * one window of the packed reference, both directions, fits 3/4 of the L2).
  * The gate writes each flag at the anchor's raw position.  Needs a matrix the
@@ -265,32 +277,45 @@ int hspz_compact_noalloc(const uint8_t *d_flags, uint64_t n, uint32_t id_base, u
 uint64_t hspz_compact_noalloc_max_flags(void);
 
 /* ------------------------------------------------------------------------ *
- * Exact X-drop materialization ("E. X-drop materialization", E.1-E.5).  For
- * survivor k with global id d_ids[k], the anchor d_anchors[d_ids[k] - id_base]
- * (n_anchors entries; an id outside [id_base, id_base + n_anchors) yields a
- * rejected slot) is walked right and left as in hspz_score_gate, keeping on each side the
- * EARLIEST step count n attaining the maximum (0 for the empty prefix).  Then
+ * Exact X-drop materialization ("E. X-drop materialization", E.1-E.5) against
+ * raw device sequences (base codes as for hspz_score_gate).  For survivor k
+ * with global id d_ids[k], the anchor d_anchors[d_ids[k] - id_base]
+ * (n_anchors entries; an id outside [id_base, id_base + n_anchors), or an
+ * anchor outside the sequences, yields a rejected slot) is walked right and
+ * left as in hspz_score_gate, keeping on each side the EARLIEST step count n
+ * attaining the maximum (0 for the empty prefix).  Then
  * ref_start = a_r - n_left, query_start = a_q - n_left,
  * len = n_left + n_right - 1 (closed interval start..=start+len) and
  * score = M_left + M_right (saturated at INT32_MAX).  done[k] = score >= T: an
  * accepted slot holds the record, a rejected slot is written as zeros with
  * done = 0.  d_out must be 16-byte aligned.  Any order of d_ids is allowed;
  * when the next entry is the next survivor on the same diagonal the two walks
- * share work (same records).  When the 8-base stop test is exact (xdrop >= 7
- * x the largest pair score) it uses stream-ordered scratch of 48 bytes per id
- * (at most 2^25 ids at a time) from the library's memory pool; it does not
+ * share work (same records).  n_anchors is not in the pages' call: it bounds
+ * the ids so that no id reads outside the caller's anchor array.  The call
+ * packs both sequences forward and reversed into stream-ordered scratch
+ * (about ref_len + query_len + 2 KiB bytes) and, when the 8-base stop test is
+ * exact (xdrop >= 7 x the largest pair score), takes 48 bytes per id (at most
+ * 2^25 ids at a time) more, all from the library's memory pool; it does not
  * synchronize `stream`.
  * ------------------------------------------------------------------------ */
-int hspz_materialize(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors,
-                     uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
-                     const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
+int hspz_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
+                     uint64_t n_ids, const uint8_t *d_ref, uint64_t ref_len, const uint8_t *d_query,
+                     uint64_t query_len, const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done,
+                     void *stream);
+
+/* The same materialization against the packed copies of `index` and `plan`
+ * (made from that index); only the 48 bytes per id of the exact-test mode are
+ * taken from the pool. */
+int hspz_materialize_plan(const hspz_index *index, const hspz_plan *plan, const hspz_anchor *d_anchors,
+                          uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids,
+                          const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done, void *stream);
 
 /* ---------------------------------------------------------------------------
- * hspz_materialize with the ids taken in diagonal order: the same records and
+ * hspz_materialize_plan with the ids taken in diagonal order: the same records and
  * done flags, at the same places, for any id list.  Each slice of at most
  * 2^25 ids is sorted (stable radix sort) by the anchor's diagonal
  * (reference end - query end) first, so that survivors on one diagonal
- * become neighbours and share their walks (hspz_materialize shares work only
+ * become neighbours and share their walks (hspz_materialize_plan shares work only
  * between neighbouring entries of the list).  Worth it when many survivors
  * lie on the same diagonals but apart in the list, as in repeats: the ids of
  * one query position hit many reference positions, i.e. many diagonals.

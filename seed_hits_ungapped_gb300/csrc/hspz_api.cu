@@ -527,13 +527,51 @@ int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_para
     return HSPZ_OK;
 }
 
-int hspz_score_gate(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n,
-                    const hspz_score_params *params, uint8_t *d_flags, void *stream) {
+int hspz_score_gate_plan(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n,
+                         const hspz_score_params *params, uint8_t *d_flags, void *stream) {
     if (!ix || !p || p->index != ix || (n && (!d_anchors || !d_flags))) return HSPZ_E_INVAL;
     ScoreArgs sa;
     if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
     SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = launch_gate(d_anchors, nullptr, n, r, q, sa, d_flags, (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate_plan");
+}
+
+// Packs the raw base codes of both sequences into one stream-ordered scratch
+// buffer (forward copies, and the reversed copies when `reversed`) for the
+// raw-sequence calls.  The copies are marked as holding N, so the kernels test
+// every step for N instead of reading the N count back to the host.
+static cudaError_t pack_raw_pair(const uint8_t *d_ref, uint64_t ref_len, const uint8_t *d_query, uint64_t query_len,
+                                 bool reversed, cudaStream_t st, uint32_t **buf, SeqView *r, SeqView *q) {
+    const uint64_t rw = packed_words(ref_len), qw = packed_words(query_len);
+    cudaError_t e = pool_alloc(buf, (reversed ? 2 : 1) * (rw + qw) * 4, st);
+    if (e != cudaSuccess) return e;
+    uint32_t *p = *buf;
+    *r = SeqView{p, ref_len, reversed ? p + rw + qw : nullptr, true};
+    *q = SeqView{p + rw, query_len, reversed ? p + 2 * rw + qw : nullptr, true};
+    e = launch_pack(d_ref, ref_len, 1, 0, const_cast<uint32_t *>(r->packed), rw, st);
+    if (e == cudaSuccess) e = launch_pack(d_query, query_len, 0, 0, const_cast<uint32_t *>(q->packed), qw, st);
+    if (e == cudaSuccess && reversed) e = launch_pack(d_ref, ref_len, 1, 1, const_cast<uint32_t *>(r->rev), rw, st);
+    if (e == cudaSuccess && reversed) e = launch_pack(d_query, query_len, 0, 1, const_cast<uint32_t *>(q->rev), qw, st);
+    return e;
+}
+
+int hspz_score_gate(const hspz_anchor *d_anchors, uint64_t n, const uint8_t *d_ref, uint64_t ref_len,
+                    const uint8_t *d_query, uint64_t query_len, const hspz_score_params *params, uint8_t *d_flags,
+                    void *stream) {
+    if (n && (!d_anchors || !d_flags)) return HSPZ_E_INVAL;
+    if ((ref_len && !d_ref) || (query_len && !d_query) || ref_len > kMaxSeqLen || query_len > kMaxSeqLen)
+        return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    if (!n) return HSPZ_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t *buf = nullptr;
+    SeqView r, q;
+    cudaError_t e = pack_raw_pair(d_ref, ref_len, d_query, query_len, false, st, &buf, &r, &q);
+    if (e == cudaSuccess) e = launch_gate(d_anchors, nullptr, n, r, q, sa, d_flags, st);
+    cudaError_t ef = buf ? pool_free(buf, st) : cudaSuccess;
+    if (e == cudaSuccess) e = ef;
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_score_gate");
 }
 
@@ -640,9 +678,9 @@ int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_
     return tail[0] > cap ? HSPZ_E_CAPACITY : HSPZ_OK;
 }
 
-int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n_anchors,
-                     uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids, const hspz_score_params *params,
-                     hspz_segment_pair *d_out, uint8_t *d_done, void *stream) {
+int hspz_materialize_plan(const hspz_index *ix, const hspz_plan *p, const hspz_anchor *d_anchors, uint64_t n_anchors,
+                          uint32_t id_base, const uint32_t *d_ids, uint64_t n_ids, const hspz_score_params *params,
+                          hspz_segment_pair *d_out, uint8_t *d_done, void *stream) {
     if (!ix || !p || p->index != ix) return HSPZ_E_INVAL;
     if (n_ids && (!d_anchors || !d_ids || !d_out || !d_done)) return HSPZ_E_INVAL;
     if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
@@ -651,6 +689,28 @@ int hspz_materialize(const hspz_index *ix, const hspz_plan *p, const hspz_anchor
     SeqView r{ix->d_ref, ix->ref_len, ix->d_ref_rev, ix->has_n}, q{p->d_qry, p->query_len, p->d_qry_rev, p->has_n};
     cudaError_t e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done,
                                        (cudaStream_t)stream);
+    return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize_plan");
+}
+
+int hspz_materialize(const hspz_anchor *d_anchors, uint64_t n_anchors, uint32_t id_base, const uint32_t *d_ids,
+                     uint64_t n_ids, const uint8_t *d_ref, uint64_t ref_len, const uint8_t *d_query,
+                     uint64_t query_len, const hspz_score_params *params, hspz_segment_pair *d_out, uint8_t *d_done,
+                     void *stream) {
+    if (n_ids && (!d_anchors || !d_ids || !d_out || !d_done)) return HSPZ_E_INVAL;
+    if ((ref_len && !d_ref) || (query_len && !d_query) || ref_len > kMaxSeqLen || query_len > kMaxSeqLen)
+        return HSPZ_E_INVAL;
+    if (reinterpret_cast<uintptr_t>(d_out) & 15u) return HSPZ_E_INVAL;
+    ScoreArgs sa;
+    if (make_score_args(params, &sa)) return HSPZ_E_INVAL;
+    if (!n_ids) return HSPZ_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    uint32_t *buf = nullptr;
+    SeqView r, q;
+    cudaError_t e = pack_raw_pair(d_ref, ref_len, d_query, query_len, true, st, &buf, &r, &q);
+    if (e == cudaSuccess)
+        e = launch_materialize(d_anchors, n_anchors, id_base, d_ids, n_ids, r, q, sa, d_out, d_done, st);
+    cudaError_t ef = buf ? pool_free(buf, st) : cudaSuccess;
+    if (e == cudaSuccess) e = ef;
     return e == cudaSuccess ? HSPZ_OK : cuda_fail(e, "hspz_materialize");
 }
 

@@ -121,7 +121,7 @@ class HspEngine:
         rec = self.buffer("records" + bufset, max(ns, 1), torch.int32, 4)
         done = self.buffer("done" + bufset, max(ns, 1), torch.uint8)
         if ns:
-            hspz.hspz_materialize(self.index, plan, anchors, hb, ids, ns, self.params, rec, done,
+            hspz.hspz_materialize_plan(self.index, plan, anchors, hb, ids, ns, self.params, rec, done,
                                   stream=self.stream, grouped=True)
         acc = self.buffer("accepted" + bufset, max(ns, 1), torch.int32)
         na = hspz.hspz_compact(done, ns, 0, acc, stream=self.stream) if ns else 0

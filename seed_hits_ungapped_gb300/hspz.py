@@ -36,6 +36,7 @@ EXPORTS = [
     "hspz_score_gate", "hspz_compact", "hspz_materialize", "hspz_chunk_walk_host", "hspz_kernel_launches",
     "hspz_compact_noalloc", "hspz_compact_noalloc_max_flags", "hspz_score_gate_bucketed", "hspz_process_chunk",
     "hspz_gather_records", "hspz_dedup", "hspz_release_cached_memory", "hspz_materialize_grouped",
+    "hspz_score_gate_plan", "hspz_materialize_plan",
 ]
 
 
@@ -87,9 +88,12 @@ def load_library():
         "hspz_plan_prefix": (ctypes.c_int, [VP, P(VP)]),
         "hspz_expand": (ctypes.c_int, [VP, U32, ctypes.c_int, VP, U64, VP]),
         "hspz_expand_gate": (ctypes.c_int, [VP, U32, P(hspz_score_params), VP, VP, U64, VP]),
-        "hspz_score_gate": (ctypes.c_int, [VP, VP, VP, U64, P(hspz_score_params), VP, VP]),
+        "hspz_score_gate": (ctypes.c_int, [VP, U64, VP, U64, VP, U64, P(hspz_score_params), VP, VP]),
+        "hspz_score_gate_plan": (ctypes.c_int, [VP, VP, VP, U64, P(hspz_score_params), VP, VP]),
         "hspz_compact": (ctypes.c_int, [VP, U64, U32, VP, U64, P(U64), VP]),
-        "hspz_materialize": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
+        "hspz_materialize": (ctypes.c_int, [VP, U64, U32, VP, U64, VP, U64, VP, U64, P(hspz_score_params), VP, VP,
+                                            VP]),
+        "hspz_materialize_plan": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
         "hspz_materialize_grouped": (ctypes.c_int, [VP, VP, VP, U64, U32, VP, U64, P(hspz_score_params), VP, VP, VP]),
         "hspz_chunk_walk_host": (ctypes.c_int, [VP, U64, U64, ctypes.c_int, P(hspz_chunk), U32, P(U32)]),
         "hspz_gather_records": (ctypes.c_int, [VP, VP, U64, VP, VP]),
@@ -287,13 +291,28 @@ def hspz_expand_gate(plan: Plan, chunk: int, params: hspz_score_params, d_anchor
     _check(rc, "hspz_expand_gate")
 
 
-def hspz_score_gate(index: Index, plan: Plan, d_anchors, n: int, params: hspz_score_params, d_flags, stream=None):
+def hspz_score_gate(d_anchors, n: int, d_ref, d_query, params: hspz_score_params, d_flags, stream=None):
+    """Gate n anchors against raw device sequences (uint8 base codes)."""
     import torch
     if d_anchors.numel() < 2 * n or d_flags.numel() < n:
         raise ValueError("buffers shorter than n")
-    rc = load_library().hspz_score_gate(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"), int(n),
+    rc = load_library().hspz_score_gate(_dptr(d_anchors, torch.int32, "d_anchors"), int(n),
+                                        _dptr(d_ref, torch.uint8, "d_ref"), d_ref.numel(),
+                                        _dptr(d_query, torch.uint8, "d_query"), d_query.numel(),
                                         ctypes.byref(params), _dptr(d_flags, torch.uint8, "d_flags"), _stream(stream))
     _check(rc, "hspz_score_gate")
+
+
+def hspz_score_gate_plan(index: Index, plan: Plan, d_anchors, n: int, params: hspz_score_params, d_flags,
+                         stream=None):
+    """Gate n anchors against the packed sequences of an index and its plan."""
+    import torch
+    if d_anchors.numel() < 2 * n or d_flags.numel() < n:
+        raise ValueError("buffers shorter than n")
+    rc = load_library().hspz_score_gate_plan(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"),
+                                             int(n), ctypes.byref(params), _dptr(d_flags, torch.uint8, "d_flags"),
+                                             _stream(stream))
+    _check(rc, "hspz_score_gate_plan")
 
 
 def hspz_score_gate_bucketed(index: Index, plan: Plan, d_anchors, n: int, params: hspz_score_params, d_flags,
@@ -370,19 +389,35 @@ def hspz_compact_noalloc(d_flags, n: int, id_base: int, d_ids, stream=None) -> i
     return out.value
 
 
-def hspz_materialize(index: Index, plan: Plan, d_anchors, id_base: int, d_ids, n_ids: int,
-                     params: hspz_score_params, d_out, d_done, stream=None, grouped: bool = False):
-    """grouped=True calls hspz_materialize_grouped (ids taken in diagonal order)."""
+def hspz_materialize(d_anchors, id_base: int, d_ids, n_ids: int, d_ref, d_query, params: hspz_score_params,
+                     d_out, d_done, stream=None):
+    """Materialize survivors against raw device sequences (uint8 base codes)."""
+    import torch
+    if d_ids.numel() < n_ids or d_out.numel() < 4 * n_ids or d_done.numel() < n_ids:
+        raise ValueError("buffers shorter than n_ids")
+    rc = load_library().hspz_materialize(_dptr(d_anchors, torch.int32, "d_anchors"), d_anchors.numel() // 2,
+                                         int(id_base), _dptr(d_ids, torch.int32, "d_ids"), int(n_ids),
+                                         _dptr(d_ref, torch.uint8, "d_ref"), d_ref.numel(),
+                                         _dptr(d_query, torch.uint8, "d_query"), d_query.numel(),
+                                         ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
+                                         _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
+    _check(rc, "hspz_materialize")
+
+
+def hspz_materialize_plan(index: Index, plan: Plan, d_anchors, id_base: int, d_ids, n_ids: int,
+                          params: hspz_score_params, d_out, d_done, stream=None, grouped: bool = False):
+    """Materialize against the packed sequences of an index and its plan;
+    grouped=True calls hspz_materialize_grouped (ids taken in diagonal order)."""
     import torch
     if d_ids.numel() < n_ids or d_out.numel() < 4 * n_ids or d_done.numel() < n_ids:
         raise ValueError("buffers shorter than n_ids")
     lib = load_library()
-    fn = lib.hspz_materialize_grouped if grouped else lib.hspz_materialize
+    fn = lib.hspz_materialize_grouped if grouped else lib.hspz_materialize_plan
     rc = fn(index.handle, plan.handle, _dptr(d_anchors, torch.int32, "d_anchors"),
             d_anchors.numel() // 2, int(id_base), _dptr(d_ids, torch.int32, "d_ids"), int(n_ids),
             ctypes.byref(params), _dptr(d_out, torch.int32, "d_out"),
             _dptr(d_done, torch.uint8, "d_done"), _stream(stream))
-    _check(rc, "hspz_materialize_grouped" if grouped else "hspz_materialize")
+    _check(rc, "hspz_materialize_grouped" if grouped else "hspz_materialize_plan")
 
 
 def hspz_release_cached_memory():

@@ -174,7 +174,7 @@ def test_fast_gate_both_step_tests(torch_cuda, name, scale, xdrop, K):
     for g in gpu.per_chunk:
         anchors = torch_cuda.from_numpy(g.anchors.view(np.int32)).cuda()
         flags = torch_cuda.zeros(len(g.anchors), dtype=torch_cuda.uint8, device="cuda")
-        hspz.hspz_score_gate(eng.index, plan, anchors, len(g.anchors), eng.params, flags)
+        hspz.hspz_score_gate_plan(eng.index, plan, anchors, len(g.anchors), eng.params, flags)
         assert np.array_equal(flags.cpu().numpy(), g.flags)
     plan.close()
 
@@ -218,7 +218,7 @@ def test_expansion_mappings_and_standalone_gate(torch_cuda):
         hspz.hspz_expand(plan, 0, a, mode)
         assert torch.equal(a, fused)
     f2 = torch.full((n,), 7, dtype=torch.uint8, device="cuda")
-    hspz.hspz_score_gate(eng.index, plan, fused, n, eng.params, f2)
+    hspz.hspz_score_gate_plan(eng.index, plan, fused, n, eng.params, f2)
     assert torch.equal(f2, flags)
 
 
@@ -390,7 +390,7 @@ def test_materialize_any_id_order(torch_cuda):
             for grouped in (False, True):
                 out = torch.full((max(k, 1), 4), -3, dtype=torch.int32, device="cuda")
                 done = torch.full((max(k, 1),), 9, dtype=torch.uint8, device="cuda")
-                hspz.hspz_materialize(eng.index, plan, anchors, base, d_ids, k, eng.params, out, done,
+                hspz.hspz_materialize_plan(eng.index, plan, anchors, base, d_ids, k, eng.params, out, done,
                                       grouped=grouped)
                 assert np.array_equal(done[:k].cpu().numpy(), done_o)
                 assert np.array_equal(out[:k].cpu().numpy(), rec_o)

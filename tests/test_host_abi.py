@@ -78,5 +78,17 @@ def test_argument_checks_without_gpu(lib):
     out = ctypes.c_uint64(7)
     assert lib.hspz_compact(None, 0, 0, None, 0, ctypes.byref(out), None) == hspz.HSPZ_OK and out.value == 0
     assert lib.hspz_compact(None, 5, 0, None, 0, ctypes.byref(out), None) == hspz.HSPZ_E_INVAL
-    assert lib.hspz_materialize(None, None, None, 0, 0, None, 0, None, None, None, None) == hspz.HSPZ_E_INVAL
+    assert lib.hspz_materialize_plan(None, None, None, 0, 0, None, 0, None, None, None, None) == hspz.HSPZ_E_INVAL
+    # the raw-sequence gate and materializer check their arguments before any CUDA call
+    params = hspz.score_params(np.eye(5, dtype=np.int32), 10, 3)
+    P = ctypes.byref(params)
+    assert lib.hspz_score_gate(None, 0, None, 0, None, 0, None, None, None) == hspz.HSPZ_E_INVAL  # no params
+    assert lib.hspz_score_gate(None, 0, None, 0, None, 0, P, None, None) == hspz.HSPZ_OK  # nothing to gate
+    assert lib.hspz_score_gate(None, 5, None, 0, None, 0, P, None, None) == hspz.HSPZ_E_INVAL  # no anchors
+    assert lib.hspz_score_gate(None, 0, None, 10, None, 0, P, None, None) == hspz.HSPZ_E_INVAL  # no reference
+    assert lib.hspz_materialize(None, 0, 0, None, 0, None, 0, None, 0, None, None, None, None) == hspz.HSPZ_E_INVAL
+    assert lib.hspz_materialize(None, 0, 0, None, 0, None, 0, None, 0, P, None, None, None) == hspz.HSPZ_OK
+    assert lib.hspz_materialize(None, 0, 0, None, 3, None, 0, None, 0, P, None, None, None) == hspz.HSPZ_E_INVAL
+    bad = hspz.score_params(np.eye(5, dtype=np.int32), -1, 3)  # negative X-drop
+    assert lib.hspz_score_gate(None, 0, None, 0, None, 0, ctypes.byref(bad), None, None) == hspz.HSPZ_E_INVAL
     assert lib.hspz_strerror(hspz.HSPZ_E_HIT_OVERFLOW).decode().startswith("total hits")
