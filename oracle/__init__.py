@@ -78,6 +78,8 @@ def _load():
             lib.orc_materialize.restype = None
             lib.orc_dedup.argtypes = [P, U64, P]
             lib.orc_dedup.restype = ctypes.c_int
+            lib.orc_fnv1a64.argtypes = [U64, P, U64]
+            lib.orc_fnv1a64.restype = U64
             _lib = lib
     return _lib
 
@@ -302,3 +304,14 @@ def run_path(ref, qry, matrix, xdrop: int, K: int, max_hits: int = 0, pattern: s
     res["final_idx"] = np.flatnonzero(keep).astype(np.uint32)
     res["final_rec"] = accepted_rec[keep.astype(bool)]
     return res
+
+
+FNV64_OFFSET = 14695981039346656037
+
+
+def fnv1a64(data, h: int = FNV64_OFFSET) -> int:
+    """FNV-1a 64-bit digest of an array's bytes (or bytes), continuing from h.
+    A test tool, not part of the method (see orc_fnv1a64)."""
+    a = np.ascontiguousarray(np.frombuffer(data, np.uint8) if isinstance(data, (bytes, bytearray)) else data)
+    b = a.reshape(-1).view(np.uint8)
+    return int(_load().orc_fnv1a64(int(h), _p(b), b.size))

@@ -475,3 +475,19 @@ int orc_dedup(const int32_t *rec, uint64_t n, uint8_t *keep)
     free(order);
     return ORC_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * FNV-1a, 64-bit (Fowler, Noll and Vo): starting from h, for every byte b in
+ * order, h = (h XOR b) * 1099511628211 mod 2^64.  The standard digest starts
+ * from the offset basis 14695981039346656037.  Not part of the method: the
+ * tests use it to compare the oracle's arrays with the CUDA path's arrays
+ * at full size, segment by segment, without holding both in memory.
+ * ------------------------------------------------------------------------- */
+uint64_t orc_fnv1a64(uint64_t h, const uint8_t *p, uint64_t n)
+{
+    for (uint64_t i = 0; i < n; i++) {
+        h ^= (uint64_t)p[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}

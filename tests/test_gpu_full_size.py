@@ -3,11 +3,13 @@ benchmark uses (the fused expansion + gate, compaction and materializer run
 chunk by chunk through the C ABI).
 
 Integer work throughout, so every compared value is bit-exact.  mid is
-compared element by element.  dense (2.1e9 anchors), workload_a and chunking
-(27 chunks over both strands) are compared on the full prefix and chunk list,
-on anchors, flags and records sampled and recomputed one by one by the oracle,
-and on properties that hold at any size: survivor ids are exactly the set
-flags in increasing order, and every sampled survivor passes the oracle gate.
+compared element by element.  workload_a, chunking (27 chunks over both
+strands) and dense (2.1e9 anchors) are compared on the full prefix and chunk
+list and, for every anchor, on digests: each chunk is cut into seed-aligned
+segments of about 2^23 anchors, the oracle computes each segment's anchors,
+flags, survivor ids, SegmentPairs and done flags in a pool of processes, and
+the FNV-1a 64 digest of each of those arrays must equal the digest of the
+same segment of the CUDA path's arrays.
 """
 import numpy as np
 import pytest
@@ -32,55 +34,92 @@ def _u32(t):
     return t.cpu().numpy().view(np.uint32)
 
 
-def sampled_parity(torch, w, n_sample=20_000, n_mat=3_000, seed=0):
+def digest_parity(torch, w, seg_anchors=1 << 23):
+    """Every anchor, flag, survivor id, SegmentPair and done flag of the
+    workload, compared by digest.  The oracle's side runs in a pool of
+    processes (spawn), one seed-aligned segment of a chunk per job; the CUDA
+    side runs each chunk through the C ABI as the benchmark does, and the
+    test digests the same segment of each device array on the host.  Returns
+    the number of anchors compared."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+    import tempfile
+
+    from oracle import digest
     from seed_hits_ungapped_gb300 import hspz
     from seed_hits_ungapped_gb300.engine import HspEngine
-    rng = np.random.default_rng(seed)
-    eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
+    T = oracle.keep_threshold(w.K)
     idx, pos = oracle.build_index(w.ref)
     checked = 0
-    for qry in w.queries:
-        buckets = oracle.seed_buckets(qry)
-        P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, buckets))
-        assert rc == 0
-        plan = eng.plan(torch.from_numpy(qry).cuda(), w.max_hits)
-        assert plan.total_hits == total
-        assert np.array_equal(_u32(plan.prefix()), P)
-        assert np.array_equal(plan.chunks, oracle.chunk_walk(P, w.max_hits))
-        for c in range(plan.n_chunks):
-            hb, he = int(plan.chunks[c, 2]), int(plan.chunks[c, 3])
-            n = he - hb
-            anchors = eng.buffer("anchors", n, torch.int32, 2)
-            flags = eng.buffer("flags", n, torch.uint8)
-            hspz.hspz_expand_gate(plan, c, eng.params, anchors, flags)
-            # sampled anchors and flags, one by one by the oracle
-            pick = np.unique(rng.integers(0, n, min(n, n_sample)))
-            pick_t = torch.from_numpy(pick.astype(np.int64)).cuda()
-            got_a = _u32(anchors[pick_t]).reshape(-1, 2)
-            want_a = oracle.anchors_at(idx, pos, buckets, P, pick + hb)
-            assert np.array_equal(got_a, want_a)
-            got_f = flags[pick_t].cpu().numpy()
-            assert np.array_equal(got_f, oracle.gate(w.ref, qry, want_a, w.matrix, w.xdrop, eng.T))
-            # survivors = the set flags, in order (checked on the device)
-            ids, n_surv = eng._compact(flags, n, hb, "ids")
-            want_ids = torch.nonzero(flags[:n]).flatten().to(torch.int64) + hb
-            assert n_surv == want_ids.numel()
-            assert torch.equal(ids[:n_surv].to(torch.int64) & 0xFFFFFFFF, want_ids)
-            if n_surv:
-                rec = eng.buffer("records", n_surv, torch.int32, 4)
-                done = eng.buffer("done", n_surv, torch.uint8)
-                hspz.hspz_materialize(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
-                sp = np.unique(rng.integers(0, n_surv, min(n_surv, n_mat)))
-                sp_t = torch.from_numpy(sp.astype(np.int64)).cuda()
-                sid = _u32(ids[sp_t])
-                sa = oracle.anchors_at(idx, pos, buckets, P, sid)
-                assert oracle.gate(w.ref, qry, sa, w.matrix, w.xdrop, eng.T).all()
-                want_rec, want_done = oracle.materialize(w.ref, qry, sa, 0, np.arange(sp.size, dtype=np.uint32),
-                                                         w.matrix, w.xdrop, eng.T)
-                assert np.array_equal(rec[sp_t].cpu().numpy(), want_rec)
-                assert np.array_equal(done[sp_t].cpu().numpy(), want_done)
-            checked += n
-        plan.close()
+    with tempfile.TemporaryDirectory() as folder:
+        np.save(os.path.join(folder, "ref.npy"), w.ref)
+        np.save(os.path.join(folder, "idx.npy"), idx)
+        np.save(os.path.join(folder, "pos.npy"), pos)
+        np.save(os.path.join(folder, "meta.npy"), np.zeros(1))
+        strands, jobs = [], []
+        for k, q in enumerate(w.queries):
+            b = oracle.seed_buckets(q)
+            P, total, rc = oracle.inclusive_prefix(oracle.count_hits(idx, b))
+            assert rc == 0
+            for name, a in (("query", q), ("buckets", b), ("P", P)):
+                np.save(os.path.join(folder, "%s%d.npy" % (name, k)), a)
+            chunks = oracle.chunk_walk(P, w.max_hits)
+            strands.append((P, total, chunks))
+            for ci, c in enumerate(chunks):
+                for seg in digest.segments(P, c, seg_anchors):
+                    jobs.append(((k, ci), seg))
+        work = [(folder, k, seg, w.matrix, w.xdrop, T, 19) for (k, _), seg in jobs]
+        n_cpu = os.cpu_count() or 4
+        with mp.get_context("spawn").Pool(n_cpu) as pool, cf.ThreadPoolExecutor(n_cpu) as hashers:
+            want = pool.map_async(digest.segment_digests, work, chunksize=1)
+            got = []
+            eng = HspEngine(w.ref, w.matrix, w.xdrop, w.K)
+            for k, q in enumerate(w.queries):
+                P, total, chunks = strands[k]
+                plan = eng.plan(torch.from_numpy(q).cuda(), w.max_hits)
+                assert plan.total_hits == total
+                assert np.array_equal(_u32(plan.prefix()), P)
+                assert np.array_equal(plan.chunks, chunks)
+                for ci in range(plan.n_chunks):
+                    hb, he = int(plan.chunks[ci, 2]), int(plan.chunks[ci, 3])
+                    n = he - hb
+                    anchors = eng.buffer("anchors", n, torch.int32, 2)
+                    flags = eng.buffer("flags", n, torch.uint8)
+                    hspz.hspz_expand_gate(plan, ci, eng.params, anchors, flags)
+                    ids, n_surv = eng._compact(flags, n, hb, "ids")
+                    rec = eng.buffer("records", max(n_surv, 1), torch.int32, 4)
+                    done = eng.buffer("done", max(n_surv, 1), torch.uint8)
+                    if n_surv:
+                        hspz.hspz_materialize_plan(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
+                    acc, n_acc = eng._compact(done, n_surv, 0, "accepted")
+                    assert n_acc == int(done[:n_surv].sum())
+                    if n_surv < (1 << 30):
+                        assert torch.equal(acc[:n_acc].long(), torch.nonzero(done[:n_surv]).flatten())
+                    k0 = 0
+                    futures = []
+                    for (kk, cc), (s0, s1, h0, h1) in jobs:
+                        if (kk, cc) != (k, ci):
+                            continue
+                        a0, a1 = h0 - hb, h1 - hb
+                        ns = int(flags[a0:a1].sum())
+                        host = [anchors[a0:a1].cpu().numpy(), flags[a0:a1].cpu().numpy(),
+                                ids[k0:k0 + ns].cpu().numpy(), rec[k0:k0 + ns].cpu().numpy(),
+                                done[k0:k0 + ns].cpu().numpy()]
+                        futures.append((a1 - a0, ns, [hashers.submit(oracle.fnv1a64, h) for h in host]))
+                        k0 += ns
+                    assert k0 == n_surv
+                    for na, ns, fs in futures:
+                        got.append((na, ns, [f.result() for f in fs]))
+                    checked += n
+                plan.close()
+            want = want.get()
+    assert len(got) == len(want) == len(jobs)
+    names = ["anchors", "flags", "ids", "records", "done"]
+    for (key, seg), (na, ns, dg), wd in zip(jobs, got, want):
+        assert (na, ns) == (wd["n_anchors"], wd["n_survivors"]), (key, seg)
+        for name, d in zip(names, dg):
+            assert d == wd[name], (name, key, seg)
     return checked
 
 
@@ -99,11 +138,11 @@ def test_mid_full_size_elementwise(torch_cuda):
             assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("name", ["dense", "workload_a", "chunking"])
-def test_full_size_sampled(torch_cuda, name):
+@pytest.mark.parametrize("name", ["workload_a", "chunking", "dense"])
+def test_full_size_digest(torch_cuda, name):
     w = synth.make(name)
-    checked = sampled_parity(torch_cuda, w)
-    assert checked > 100_000_000
+    checked = digest_parity(torch_cuda, w)
+    assert checked > 200_000_000
     from seed_hits_ungapped_gb300 import hspz
     hspz.hspz_release_cached_memory()
     torch_cuda.cuda.empty_cache()

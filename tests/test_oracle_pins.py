@@ -573,3 +573,52 @@ def test_gate_flags_match_prefix_sum_form(seed, X):
         T = max(T, 1)
         flags = oracle.gate(ref, qry, anchors, m, X, T)
         assert flags.tolist() == (tot >= T).astype(np.uint8).tolist()
+
+
+# ---------------------------------------------------------------- digests (test tool, not the method)
+
+def test_fnv1a64_published_vectors_and_streaming():
+    """FNV-1a 64 (Fowler, Noll, Vo): the published digests of "", "a" and
+    "foobar"; a digest continued over pieces equals the digest of the whole."""
+    assert oracle.fnv1a64(b"") == 0xCBF29CE484222325
+    assert oracle.fnv1a64(b"a") == 0xAF63DC4C8601EC8C
+    assert oracle.fnv1a64(b"foobar") == 0x85944171F73967E8
+    data = np.random.default_rng(3).integers(0, 256, 1000).astype(np.uint8)
+    h = oracle.fnv1a64(data[:300])
+    assert oracle.fnv1a64(data[300:], h) == oracle.fnv1a64(data)
+    assert oracle.fnv1a64(data.view(np.uint32)) == oracle.fnv1a64(data)
+
+
+def test_segment_digests_equal_whole_chunk_arrays(tmp_path):
+    """The per-segment oracle pass used for full-size parity gives, segment by
+    segment, the digests of the slices of the whole-chunk oracle arrays."""
+    from oracle import digest
+    from seed_hits_ungapped_gb300 import synth
+    w = synth.make("chunking", scale=0.02)
+    res = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K, max_hits=w.max_hits)
+    idx, pos = res["idx"], res["pos"]
+    np.save(tmp_path / "ref.npy", w.ref)
+    np.save(tmp_path / "idx.npy", idx)
+    np.save(tmp_path / "pos.npy", pos)
+    np.save(tmp_path / "meta.npy", np.zeros(1))
+    np.save(tmp_path / "query0.npy", w.query)
+    np.save(tmp_path / "buckets0.npy", res["buckets"])
+    np.save(tmp_path / "P0.npy", res["P"])
+    assert len(res["chunks"]) > 2
+    n_seg = 0
+    for c, pc in zip(res["chunks"], res["per_chunk"]):
+        hb = int(c[2])
+        segs = digest.segments(res["P"], c, 997)
+        assert segs[0][0] == c[0] and segs[-1][1] == c[1]
+        for s0, s1, h0, h1 in segs:
+            got = digest.segment_digests((str(tmp_path), 0, (s0, s1, h0, h1), w.matrix, w.xdrop, res["T"], SPAN))
+            a0, a1 = h0 - hb, h1 - hb
+            sel = (pc["ids"] >= h0) & (pc["ids"] < h1)
+            assert got["n_anchors"] == a1 - a0 and got["n_survivors"] == int(sel.sum())
+            assert got["anchors"] == oracle.fnv1a64(pc["anchors"][a0:a1])
+            assert got["flags"] == oracle.fnv1a64(pc["flags"][a0:a1])
+            assert got["ids"] == oracle.fnv1a64(pc["ids"][sel])
+            assert got["records"] == oracle.fnv1a64(pc["rec"][sel])
+            assert got["done"] == oracle.fnv1a64(pc["done"][sel])
+            n_seg += 1
+    assert n_seg > 6
