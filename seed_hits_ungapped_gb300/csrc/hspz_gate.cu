@@ -200,22 +200,31 @@ constexpr int kLeadLeft = HSPZ_LEAD_LEFT, kLeadRight = HSPZ_LEAD_RIGHT;
 // otherwise flagged steps are settled by walk_resolve, together, after every
 // lane has flagged.  Leaves the side maximum in w.M and returns whether it
 // reached `need`.
+// The LEAD branch-free steps of one side (exact stop test), for the lanes
+// with `walk`.  Afterwards w.rem = 0 for a lane whose side is over (stop,
+// `need` reached, edge or no walk); otherwise the lane's side goes on from
+// LEAD words past its start with w.rem bases left.
+template <bool HAS_N, bool BACK, int LEAD>
+__device__ __forceinline__ void side_lead(WalkState &w, bool walk, uint32_t tlo, uint32_t thi,
+                                          const int *__restrict__ tab, int X, int need) {
+    if (!walk) w.rem = 0;
+    if (__all_sync(kFullMask, w.rem == 0u || w.rem > 8u * LEAD)) {
+        // no walk of the round can reach its edge during the lead steps
+        uint32_t keep = w.rem ? 0xFFFFFFFFu : 0u;
+#pragma unroll
+        for (int i = 0; i < LEAD; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
+        w.rem = keep ? w.rem - 8u * LEAD : 0u;
+    } else {
+#pragma unroll
+        for (int i = 0; i < LEAD; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
+    }
+}
+
 template <bool HAS_N, bool EXACT, bool BACK>
 __device__ __forceinline__ bool gate_side(WalkState &w, bool walk, uint32_t tlo, uint32_t thi,
                                           const int *__restrict__ tab, int X, int need) {
     if (EXACT) {
-        constexpr int lead = BACK ? kLeadLeft : kLeadRight;
-        if (!walk) w.rem = 0;
-        if (__all_sync(kFullMask, w.rem == 0u || w.rem > 8u * lead)) {
-            // no walk of the round can reach its edge during the lead steps
-            uint32_t keep = w.rem ? 0xFFFFFFFFu : 0u;
-#pragma unroll
-            for (int i = 0; i < lead; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
-            w.rem = keep ? w.rem - 8u * lead : 0u;
-        } else {
-#pragma unroll
-            for (int i = 0; i < lead; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
-        }
+        side_lead<HAS_N, BACK, BACK ? kLeadLeft : kLeadRight>(w, walk, tlo, thi, tab, X, need);
         // the tail: the same steps under a warp vote, while any lane walks
         while (__any_sync(kFullMask, w.rem != 0)) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
         return walk && w.M >= need;
@@ -276,6 +285,85 @@ __device__ __forceinline__ bool gate_round(uint2 a, bool walk0, const Seqs &sq, 
     return accepted;
 }
 
+// Right-side lead steps of a round whose long right walks are deferred.
+#ifndef HSPZ_DEFER_RIGHT
+#define HSPZ_DEFER_RIGHT 4
+#endif
+constexpr int kDeferRight = HSPZ_DEFER_RIGHT;
+constexpr int kQueue = 64;  // deferred right walks a warp can hold (one round adds at most 32)
+
+// gate_round for the exact step test, except that a right walk still going
+// after kDeferRight steps is not finished here: *pending is set and the
+// walk's running sum and maximum (w.S, w.M) and the maximum it still needs
+// (*need) are left for gate_deferred.  A round lasts its slowest walk, and
+// right walks mostly end within 2-4 steps while a few run much longer, so
+// finishing those few together, 32 at a time, keeps the other lanes busy.
+template <bool HAS_N>
+__device__ __forceinline__ bool gate_round_defer(uint2 a, bool walk0, const Seqs &sq, uint32_t tlo, uint32_t thi,
+                                                 const int *__restrict__ tab, int X, int T, WalkState &w,
+                                                 int &need, bool &pending) {
+    w = WalkState{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t nr1 = 0, nq1 = 0;
+    if (walk0) {
+        walk_place_fwd(w, sq, a.x, a.y, 0);
+        w.r0 = __ldg(w.pr);
+        w.r1 = __ldg(w.pr + 1);
+        w.q0 = __ldg(w.pq);
+        w.q1 = __ldg(w.pq + 1);
+        nr1 = __ldg(w.pr + 2);
+        nq1 = __ldg(w.pq + 2);
+    }
+    const uint32_t nr0 = w.r1, nq0 = w.q1;
+    bool accepted = gate_side<HAS_N, true, true>(w, walk0, tlo, thi, tab, X, T);
+    need = T - w.M;
+    const bool walk1 = walk0 && !accepted;
+    if (walk1) {
+        walk_place_fwd(w, sq, a.x, a.y, 1);
+        w.r0 = nr0;
+        w.r1 = nr1;
+        w.q0 = nq0;
+        w.q1 = nq1;
+    }
+    side_lead<HAS_N, false, kDeferRight>(w, walk1, tlo, thi, tab, X, need);
+    pending = w.rem != 0;
+    return accepted | (walk1 && w.M >= need);
+}
+
+// Finishes `cnt` deferred right walks (queue entries first .. first+cnt-1,
+// one per lane) and writes their flags: each walk is placed again
+// kDeferRight words past the anchor with its saved sum and maximum, then all
+// step together under a warp vote.
+template <bool HAS_N>
+__device__ __forceinline__ void gate_deferred(const uint32_t *qslot, const int *qS, const int *qM, const int *qN,
+                                              uint32_t first, uint32_t cnt, const uint2 *sA, const Seqs &sq,
+                                              uint32_t tlo, uint32_t thi, const int *__restrict__ tab, int X,
+                                              uint8_t *__restrict__ flags) {
+    const int lane = threadIdx.x & 31;
+    const bool mine = (uint32_t)lane < cnt;
+    WalkState w{sq.ref, sq.qry, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t ai = 0;
+    int need = 0;
+    if (mine) {
+        const uint32_t e = first + (uint32_t)lane;
+        ai = qslot[e];
+        need = qN[e];
+        const uint2 a = sA[ai];
+        walk_place_fwd(w, sq, a.x, a.y, 1);
+        w.pr += kDeferRight;
+        w.pq += kDeferRight;
+        w.rem -= 8u * kDeferRight;
+        w.S = qS[e];
+        w.M = qM[e];
+        w.r0 = __ldg(w.pr);
+        w.r1 = __ldg(w.pr + 1);
+        w.q0 = __ldg(w.pq);
+        w.q1 = __ldg(w.pq + 1);
+    }
+    __syncwarp();  // every entry is read before the queue is written again
+    while (__any_sync(kFullMask, w.rem != 0)) walk_step_lead<HAS_N, false>(w, tlo, thi, tab, X, need);
+    if (mine) __stcs(flags + ai, (uint8_t)(w.M >= need ? 1 : 0));
+}
+
 #ifndef HSPZ_GATE_MIN_BLOCKS
 #define HSPZ_GATE_MIN_BLOCKS 10  // resident CTAs per SM the register budget allows
 #endif
@@ -326,8 +414,9 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
         for (uint32_t i = tid; i < ns; i += kWWarps * 32) sP[i] = __ldg(P + first + i);
     __syncthreads();
     const uint32_t wbase = (uint32_t)warp * kWUnit;  // this warp's slots within the tile
-    if (wbase >= tile_count) return;
-    const uint32_t count = min((uint32_t)kWUnit, tile_count - wbase);
+    // with EXACT every warp reaches the barrier after the expansion, even one without slots
+    if (!EXACT && wbase >= tile_count) return;
+    const uint32_t count = wbase < tile_count ? min((uint32_t)kWUnit, tile_count - wbase) : 0u;
     const uint64_t t0 = tile0 + wbase;
     uint2 *sA = sA_all + wbase;
 
@@ -359,18 +448,58 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
             sA[i0 + k] = make_uint2(__ldcs(pos + base + (pend - 1 - g)), first + l + span - 1);
         }
     }
-    __syncwarp();
-
-    // 2. gate rounds
     const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
     const int X = sa.xdrop, T = sa.T;
-    for (uint32_t round = 0; round * 32 < count; round++) {
-        const uint32_t ai = round * 32u + (uint32_t)lane;
-        const bool valid = ai < count;
-        uint2 a = make_uint2(0, 0);
-        if (valid) a = sA[ai];
-        const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, tlo, thi, tab, X, T);
-        if (valid) __stcs(flags + t0 + ai, (uint8_t)(accepted ? 1 : 0));
+    if (EXACT) {
+        // 2. gate rounds with deferred right walks.  After this barrier no warp
+        // reads the seed prefixes again, so each warp's quarter of sP becomes its
+        // queue of deferred walks (slot, running sum, maximum, needed maximum).
+        __syncthreads();
+        if (!count) return;
+        uint32_t *qslot = sP + (uint32_t)warp * (kWSeeds / kWWarps);
+        int *qS = reinterpret_cast<int *>(qslot + kQueue), *qM = qS + kQueue, *qN = qM + kQueue;
+        const uint32_t lane_lt = (1u << lane) - 1u;
+        uint32_t qn = 0;  // warp-uniform queue length
+        for (uint32_t round = 0; round * 32 < count; round++) {
+            const uint32_t ai = round * 32u + (uint32_t)lane;
+            const bool valid = ai < count;
+            uint2 a = make_uint2(0, 0);
+            if (valid) a = sA[ai];
+            WalkState w;
+            int need;
+            bool pending;
+            const bool accepted = gate_round_defer<HAS_N>(a, valid, sq, tlo, thi, tab, X, T, w, need, pending);
+            if (valid && !pending) __stcs(flags + t0 + ai, (uint8_t)(accepted ? 1 : 0));
+            const uint32_t pb = __ballot_sync(kFullMask, pending);
+            if (pending) {
+                const uint32_t e = qn + __popc(pb & lane_lt);
+                qslot[e] = ai;
+                qS[e] = w.S;
+                qM[e] = w.M;
+                qN[e] = need;
+            }
+            qn += __popc(pb);
+            if (qn >= 32) {
+                __syncwarp();
+                gate_deferred<HAS_N>(qslot, qS, qM, qN, qn - 32, 32, sA, sq, tlo, thi, tab, X, flags + t0);
+                qn -= 32;
+            }
+        }
+        if (qn) {
+            __syncwarp();
+            gate_deferred<HAS_N>(qslot, qS, qM, qN, 0, qn, sA, sq, tlo, thi, tab, X, flags + t0);
+        }
+    } else {
+        __syncwarp();
+        // 2. gate rounds
+        for (uint32_t round = 0; round * 32 < count; round++) {
+            const uint32_t ai = round * 32u + (uint32_t)lane;
+            const bool valid = ai < count;
+            uint2 a = make_uint2(0, 0);
+            if (valid) a = sA[ai];
+            const bool accepted = gate_round<HAS_N, EXACT>(a, valid, sq, tlo, thi, tab, X, T);
+            if (valid) __stcs(flags + t0 + ai, (uint8_t)(accepted ? 1 : 0));
+        }
     }
     // 3. anchors
     // positions, flags and anchors stream through once (cache-streaming loads and stores),

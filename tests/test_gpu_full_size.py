@@ -38,7 +38,7 @@ def digest_parity(torch, w, seg_anchors=1 << 23):
     """Every anchor, flag, survivor id, SegmentPair and done flag of the
     workload, compared by digest.  The oracle's side runs in a pool of
     processes (spawn), one seed-aligned segment of a chunk per job; the CUDA
-    side runs each chunk through the C ABI as the benchmark does, and the
+    side runs each chunk through hspz_process_chunk as the benchmark does, and the
     test digests the same segment of each device array on the host.  Returns
     the number of anchors compared."""
     import concurrent.futures as cf
@@ -47,7 +47,6 @@ def digest_parity(torch, w, seg_anchors=1 << 23):
     import tempfile
 
     from oracle import digest
-    from seed_hits_ungapped_gb300 import hspz
     from seed_hits_ungapped_gb300.engine import HspEngine
     T = oracle.keep_threshold(w.K)
     idx, pos = oracle.build_index(w.ref)
@@ -83,16 +82,12 @@ def digest_parity(torch, w, seg_anchors=1 << 23):
                 assert np.array_equal(plan.chunks, chunks)
                 for ci in range(plan.n_chunks):
                     hb, he = int(plan.chunks[ci, 2]), int(plan.chunks[ci, 3])
-                    n = he - hb
-                    anchors = eng.buffer("anchors", n, torch.int32, 2)
-                    flags = eng.buffer("flags", n, torch.uint8)
-                    hspz.hspz_expand_gate(plan, ci, eng.params, anchors, flags)
-                    ids, n_surv = eng._compact(flags, n, hb, "ids")
-                    rec = eng.buffer("records", max(n_surv, 1), torch.int32, 4)
-                    done = eng.buffer("done", max(n_surv, 1), torch.uint8)
-                    if n_surv:
-                        hspz.hspz_materialize_plan(eng.index, plan, anchors, hb, ids, n_surv, eng.params, rec, done)
-                    acc, n_acc = eng._compact(done, n_surv, 0, "accepted")
+                    # the benchmark's launch configuration: one hspz_process_chunk per chunk
+                    n, n_surv, n_acc, _ = eng.process_chunk(plan, ci)
+                    assert n == he - hb
+                    b = eng._bufs
+                    anchors, flags, ids, rec, done, acc = (b["anchors"], b["flags"], b["ids"], b["records"],
+                                                          b["done"], b["accepted"])
                     assert n_acc == int(done[:n_surv].sum())
                     if n_surv < (1 << 30):
                         assert torch.equal(acc[:n_acc].long(), torch.nonzero(done[:n_surv]).flatten())
