@@ -13,27 +13,46 @@ __device__ __forceinline__ uint32_t pack_nibble(uint32_t c, int parity) {
     return c | (parity ? (((c ^ (c >> 1)) & 1u) << 2) : 0u);
 }
 
-// One thread per packed word: 8 bases, padded with N outside [0, len).
+// One thread per packed word: 8 bases, padded with N outside [0, len).  A
+// word whose 8 bases lie inside the sequence at an 8-byte aligned place
+// (forward: codes + 8w - padding; reversed: its mirror) takes them with one
+// 8-byte load; the others (the ends, or unaligned codes) go byte by byte.
+// N bases are counted per warp before one atomic add.
 __global__ void k_pack(const uint8_t *__restrict__ codes, uint64_t len, int parity, int reverse,
                        uint32_t *__restrict__ out, uint64_t words, unsigned long long *__restrict__ n_count) {
-    unsigned long long ns = 0;
+    uint32_t ns = 0;
+    const bool aligned = ((reinterpret_cast<uintptr_t>(reverse ? codes + len : codes)) & 7u) == 0;
     for (uint64_t w = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; w < words;
          w += (uint64_t)gridDim.x * blockDim.x) {
-        int64_t b0 = (int64_t)w * 8 - kPadBases;
+        const int64_t b0 = (int64_t)w * 8 - kPadBases;
         uint32_t v = 0;
+        if (aligned && b0 >= 0 && (uint64_t)b0 + 8 <= len) {
+            // reversed: bases b0 .. b0+7 are codes[len-1-b0] down to codes[len-8-b0]
+            const uint2 raw = *reinterpret_cast<const uint2 *>(codes + (reverse ? len - 8 - (uint64_t)b0 : (uint64_t)b0));
+            const uint32_t lo4 = reverse ? __byte_perm(raw.y, 0, 0x0123) : raw.x;
+            const uint32_t hi4 = reverse ? __byte_perm(raw.x, 0, 0x0123) : raw.y;
 #pragma unroll
-        for (int i = 0; i < 8; i++) {
-            int64_t b = b0 + i;
-            uint32_t nib = kNibN;
-            if (b >= 0 && (uint64_t)b < len) {
-                nib = pack_nibble(codes[reverse ? len - 1 - b : b], parity);
+            for (int i = 0; i < 8; i++) {
+                const uint32_t nib = pack_nibble(((i < 4 ? lo4 : hi4) >> (8 * (i & 3))) & 0xFFu, parity);
                 ns += nib == kNibN;
+                v |= nib << (4 * i);
             }
-            v |= nib << (4 * i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int64_t b = b0 + i;
+                uint32_t nib = kNibN;
+                if (b >= 0 && (uint64_t)b < len) {
+                    nib = pack_nibble(codes[reverse ? len - 1 - b : b], parity);
+                    ns += nib == kNibN;
+                }
+                v |= nib << (4 * i);
+            }
         }
         out[w] = v;
     }
-    if (n_count && ns) atomicAdd(n_count, ns);
+    ns = __reduce_add_sync(kFull, ns);
+    if (n_count && ns && (threadIdx.x & 31) == 0) atomicAdd(n_count, (unsigned long long)ns);
 }
 
 template <typename T>
