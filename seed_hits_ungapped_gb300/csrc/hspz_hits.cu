@@ -74,43 +74,68 @@ __device__ __forceinline__ T warp_sum(T x) {
 
 // find_num_hits (C.1): one thread per seed; the block also emits its 64-bit
 // count sum (C.2: 256 counts per block).
+// Four 256-seed count blocks per CTA (C.1, and the per-block sums of C.2):
+// thread t takes seeds t, t + 256, t + 512 and t + 768 of the CTA's span, so
+// its four index lookups are in flight together, and each 256 seeds get their
+// own sum in bsum.
+constexpr int kCountPer = 4;
+
 __global__ void __launch_bounds__(kCountBlock) k_count(const uint8_t *__restrict__ q, uint64_t n_seeds, SeedShape sh,
                                                        const uint32_t *__restrict__ idx, uint32_t *__restrict__ cnt,
                                                        uint32_t *__restrict__ lo, uint64_t *__restrict__ bsum) {
-    __shared__ uint8_t tile[kCountBlock + kMaxSpan];
-    __shared__ uint64_t wsum[kCountBlock / 32];
-    const uint64_t s0 = blockIdx.x * (uint64_t)kCountBlock;
+    __shared__ uint8_t tile[kCountPer * kCountBlock + kMaxSpan];
+    __shared__ uint64_t wsum[kCountPer][kCountBlock / 32];
+    const uint64_t s0 = blockIdx.x * (uint64_t)(kCountPer * kCountBlock);
     const uint64_t qlen = n_seeds + sh.span - 1;
-    for (int i = threadIdx.x; i < kCountBlock + sh.span - 1; i += blockDim.x) {
-        uint64_t p = s0 + i;
+    for (int i = threadIdx.x; i < kCountPer * kCountBlock + sh.span - 1; i += blockDim.x) {
+        const uint64_t p = s0 + i;
         tile[i] = p < qlen ? q[p] : 4;
     }
     __syncthreads();
-    const uint64_t s = s0 + threadIdx.x;
-    uint32_t c = 0, l = 0;
-    if (s < n_seeds) {
-        uint32_t h = 0;
-        bool ok = true;
-        for (int i = 0; i < sh.weight; i++) {
-            uint32_t b = tile[threadIdx.x + sh.care[i]];
-            ok &= (b <= 3);
-            h = h * 4u + (b & 3u);
+    uint32_t h[kCountPer];
+    bool ok[kCountPer];
+#pragma unroll
+    for (int k = 0; k < kCountPer; k++) {
+        const int t = threadIdx.x + k * kCountBlock;
+        uint32_t v = 0;
+        bool good = s0 + t < n_seeds;
+#pragma unroll
+        for (int i = 0; i < kMaxWeight; i++) {
+            if (i < sh.weight) {
+                const uint32_t b = tile[t + sh.care[i]];
+                good &= (b <= 3);
+                v = v * 4u + (b & 3u);
+            }
         }
-        if (ok) {
-            l = h ? __ldg(idx + h - 1) : 0u;
-            c = __ldg(idx + h) - l;
-        }
-        cnt[s] = c;
-        lo[s] = l;
+        h[k] = v;
+        ok[k] = good;
     }
-    uint64_t v = warp_sum<uint64_t>(c);
+    uint32_t end[kCountPer], prev[kCountPer];
+#pragma unroll
+    for (int k = 0; k < kCountPer; k++) {
+        end[k] = ok[k] ? __ldg(idx + h[k]) : 0u;
+        prev[k] = (ok[k] && h[k]) ? __ldg(idx + h[k] - 1) : 0u;
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (lane == 0) wsum[warp] = v;
+#pragma unroll
+    for (int k = 0; k < kCountPer; k++) {
+        const uint64_t s = s0 + threadIdx.x + k * kCountBlock;
+        const uint32_t c = end[k] - prev[k];  // 0 for a seed without a k-mer
+        if (s < n_seeds) {
+            cnt[s] = c;
+            lo[s] = prev[k];
+        }
+        const uint64_t v = warp_sum<uint64_t>(c);
+        if (lane == 0) wsum[k][warp] = v;
+    }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        uint64_t t = 0;
-        for (int w = 0; w < kCountBlock / 32; w++) t += wsum[w];
-        bsum[blockIdx.x] = t;
+    if (threadIdx.x < kCountPer) {
+        const uint64_t b = blockIdx.x * (uint64_t)kCountPer + threadIdx.x;  // the 256-seed block
+        if (b * kCountBlock < n_seeds) {
+            uint64_t t = 0;
+            for (int w = 0; w < kCountBlock / 32; w++) t += wsum[threadIdx.x][w];
+            bsum[b] = t;
+        }
     }
 }
 
@@ -416,9 +441,10 @@ cudaError_t launch_pack(const uint8_t *d_codes, uint64_t len, int with_parity, i
 
 cudaError_t launch_count(const uint8_t *d_query, uint64_t n_seeds, const SeedShape &sh, const uint32_t *d_idx,
                          uint32_t *d_cnt, uint32_t *d_lo, uint64_t *d_block_sum, cudaStream_t st) {
-    uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
+    const uint64_t nb = (n_seeds + kCountBlock - 1) / kCountBlock;
     if (!nb) return cudaSuccess;
-    k_count<<<(unsigned)nb, kCountBlock, 0, st>>>(d_query, n_seeds, sh, d_idx, d_cnt, d_lo, d_block_sum); count_launch();
+    k_count<<<(unsigned)((nb + kCountPer - 1) / kCountPer), kCountBlock, 0, st>>>(d_query, n_seeds, sh, d_idx, d_cnt,
+                                                                                   d_lo, d_block_sum); count_launch();
     return cudaGetLastError();
 }
 
