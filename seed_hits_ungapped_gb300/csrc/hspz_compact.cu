@@ -7,8 +7,8 @@ namespace hspz {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kPerThread = 16;
-constexpr int kTile = kThreads * kPerThread;  // 4096 flags per block
+constexpr int kPerThread = 64;
+constexpr int kTile = kThreads * kPerThread;  // 16384 flags per block
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // The count of flags: n, or (when d_n is given) the count at d_n if it is at
@@ -19,23 +19,29 @@ __device__ __forceinline__ uint64_t count_of(uint64_t n, const uint64_t *d_n) {
     return v <= n ? v : 0;
 }
 
-// The 16 flags a thread owns, as a 16-bit mask (bit i = flag i != 0).
+// The 64 flags a thread owns, as a 64-bit mask (bit i = flag i != 0); with
+// ALIGNED flags a full set comes in four 16-byte loads issued together.
 template <bool ALIGNED>
-__device__ __forceinline__ uint32_t load_mask(const uint8_t *__restrict__ f, uint64_t i0, uint64_t n) {
-    uint32_t m = 0;
+__device__ __forceinline__ uint64_t load_mask(const uint8_t *__restrict__ f, uint64_t i0, uint64_t n) {
+    uint64_t m = 0;
     if (ALIGNED && i0 + kPerThread <= n) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(f + i0));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint4 v[kPerThread / 16];
 #pragma unroll
-        for (int k = 0; k < 4; k++) {
-            const uint32_t nz = __vcmpne4(w[k], 0u);  // 0xFF per non-zero byte
+        for (int q = 0; q < kPerThread / 16; q++) v[q] = __ldg(reinterpret_cast<const uint4 *>(f + i0) + q);
 #pragma unroll
-            for (int b = 0; b < 4; b++) m |= ((nz >> (8 * b + 7)) & 1u) << (4 * k + b);
+        for (int q = 0; q < kPerThread / 16; q++) {
+            const uint32_t w[4] = {v[q].x, v[q].y, v[q].z, v[q].w};
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                const uint32_t nz = __vcmpne4(w[k], 0u);  // 0xFF per non-zero byte
+#pragma unroll
+                for (int b = 0; b < 4; b++) m |= (uint64_t)((nz >> (8 * b + 7)) & 1u) << (16 * q + 4 * k + b);
+            }
         }
     } else {
-#pragma unroll
+#pragma unroll 16
         for (int k = 0; k < kPerThread; k++)
-            if (i0 + k < n && f[i0 + k]) m |= 1u << k;
+            if (i0 + k < n && f[i0 + k]) m |= 1ull << k;
     }
     return m;
 }
@@ -47,7 +53,7 @@ __global__ void __launch_bounds__(kThreads) k_count_flags(const uint8_t *__restr
     __shared__ uint32_t ws[kThreads / 32];
     n = count_of(n, d_n);
     const uint64_t i0 = blockIdx.x * (uint64_t)kTile + (uint64_t)threadIdx.x * kPerThread;
-    uint32_t c = __popc(load_mask<ALIGNED>(f, i0, n));
+    uint32_t c = __popcll(load_mask<ALIGNED>(f, i0, n));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(kFull, c, o);
     if ((threadIdx.x & 31) == 0) ws[threadIdx.x >> 5] = c;
@@ -100,13 +106,15 @@ __global__ void __launch_bounds__(kThreads) k_emit(const uint8_t *__restrict__ f
                                                    const uint64_t *__restrict__ excl,
                                                    const uint64_t *__restrict__ total, uint64_t cap,
                                                    uint32_t *__restrict__ ids) {
-    if (*total > cap) return;  // nothing is written when the output does not fit
     n = count_of(n, d_n);
     __shared__ uint32_t ws[kThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint64_t i0 = blockIdx.x * (uint64_t)kTile + (uint64_t)threadIdx.x * kPerThread;
-    uint32_t m = load_mask<ALIGNED>(f, i0, n);
-    const uint32_t c = __popc(m);
+    // the flags, the block's offset and the total are independent loads: all in flight together
+    uint64_t m = load_mask<ALIGNED>(f, i0, n);
+    const uint64_t block_base = excl[blockIdx.x];
+    if (*total > cap) return;  // nothing is written when the output does not fit (the same for every block)
+    const uint32_t c = __popcll(m);
     uint32_t x = c;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -117,9 +125,9 @@ __global__ void __launch_bounds__(kThreads) k_emit(const uint8_t *__restrict__ f
     __syncthreads();
     uint32_t pre = x - c;
     for (int w = 0; w < warp; w++) pre += ws[w];
-    uint64_t dst = excl[blockIdx.x] + pre;
+    uint64_t dst = block_base + pre;
     while (m) {
-        const int b = __ffs(m) - 1;
+        const int b = __ffsll((long long)m) - 1;
         m &= m - 1;
         ids[dst++] = id_base + (uint32_t)(i0 + b);
     }

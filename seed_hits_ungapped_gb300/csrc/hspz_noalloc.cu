@@ -21,8 +21,9 @@
 namespace hspz {
 namespace {
 
-// Flags per compaction block are 4096; the scratch holds one 32-bit count
-// and one 64-bit offset per block plus the 64-bit total.
+// The scratch holds one 32-bit count and one 64-bit offset per compaction
+// block plus the 64-bit total; sized here for blocks of 4096 flags, it has
+// room to spare for the 16384-flag blocks of launch_compact.
 constexpr uint64_t kNoAllocMaxFlags = 1ull << 28;
 constexpr uint64_t kNoAllocWords = 3 * (kNoAllocMaxFlags / 4096) + 8;
 
