@@ -277,13 +277,11 @@ __global__ void __launch_bounds__(256, HSPZ_MAT_MIN_BLOCKS) k_materialize_blocks
                 const uint32_t Q = __funnelshift_r(w.q0, w.q1, w.shq);
                 int Sv[8];
                 step_sums<true, HAS_N>(R, Q, low_nibbles(w.rem), tlo, thi, tab, w.S, Sv);
-                int m = w.M, d = 0;
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    d |= Sv[j] + X - m;
-                    m = max(m, Sv[j]);
-                }
-                const bool over = (d < 0) | (w.rem <= 8);
+                // exact stop test from the step's range (X >= 7 x the largest pair score; see
+                // walk_step_lead): m is also the running maximum at the step's end
+                int m, lo;
+                step_range(Sv, w.M, m, lo);
+                const bool over = (lo + X - m < 0) | (w.rem <= 8);
                 // a join: past the neighbour and standing at the running maximum
                 const bool join = CHAIN && stepping && !over && steps >= tjoin && m == Sv[7];
                 joined |= join;
