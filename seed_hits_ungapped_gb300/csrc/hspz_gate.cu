@@ -420,7 +420,10 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     const uint64_t t0 = tile0 + wbase;
     uint2 *sA = sA_all + wbase;
 
-    // 1. expansion
+    // 1. expansion.  The lane first finds the seed and occurrence of each of
+    // its 8 slots (from the cached prefixes), then issues the 8 bucket-start
+    // loads together and then the 8 position loads together: two rounds of
+    // memory latency per lane instead of one per slot.
     const uint32_t i0 = (uint32_t)lane * 8u;
     if (i0 < count) {
         const uint32_t g0 = hb + (uint32_t)t0 + i0;
@@ -436,17 +439,26 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
             l = upper_bound_g(P, first, first + ns, g0) - first;
         }
         uint32_t pend = cached ? sP[l] : __ldg(P + first + l);
-        uint32_t base = __ldg(lo + first + l);
         const uint32_t kmax = min(8u, count - i0);
-        for (uint32_t k = 0; k < kmax; k++) {
-            const uint32_t g = g0 + k;
+        uint32_t sk[8], jk[8];
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++) {
+            const uint32_t g = g0 + min(k, kmax - 1);  // slots past the unit repeat its last one
             while (pend <= g) {
                 l++;
                 pend = cached ? sP[l] : __ldg(P + first + l);
-                base = __ldg(lo + first + l);
             }
-            sA[i0 + k] = make_uint2(__ldcs(pos + base + (pend - 1 - g)), first + l + span - 1);
+            sk[k] = l;
+            jk[k] = pend - 1 - g;
         }
+        uint32_t base[8], re[8];
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++) base[k] = __ldg(lo + first + sk[k]);
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++) re[k] = __ldcs(pos + base[k] + jk[k]);
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++)
+            if (k < kmax) sA[i0 + k] = make_uint2(re[k], first + sk[k] + span - 1);
     }
     const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
     const int X = sa.xdrop, T = sa.T;
