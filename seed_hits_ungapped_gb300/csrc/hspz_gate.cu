@@ -421,9 +421,13 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     uint2 *sA = sA_all + wbase;
 
     // 1. expansion.  The lane first finds the seed and occurrence of each of
-    // its 8 slots (from the cached prefixes), then issues the 8 bucket-start
-    // loads together and then the 8 position loads together: two rounds of
-    // memory latency per lane instead of one per slot.
+    // its 8 consecutive slots (from the cached prefixes) and issues their 8
+    // bucket-start loads together; the position indices then pass through
+    // shared memory, so that lane l loads the positions of slots l + 32k:
+    // each load instruction covers 32 consecutive anchors (a few buckets)
+    // rather than 32 buckets.  The staging words sit in the warp's anchor
+    // slots, XOR-swizzled so that both passes are free of bank conflicts.
+    uint32_t *sW = reinterpret_cast<uint32_t *>(sA);  // 2 x 256 staging words
     const uint32_t i0 = (uint32_t)lane * 8u;
     if (i0 < count) {
         const uint32_t g0 = hb + (uint32_t)t0 + i0;
@@ -451,14 +455,35 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
             sk[k] = l;
             jk[k] = pend - 1 - g;
         }
-        uint32_t base[8], re[8];
+        uint32_t base[8];
 #pragma unroll
         for (uint32_t k = 0; k < 8; k++) base[k] = __ldg(lo + first + sk[k]);
-#pragma unroll
-        for (uint32_t k = 0; k < 8; k++) re[k] = __ldcs(pos + base[k] + jk[k]);
+        const uint32_t swz = (uint32_t)(lane >> 2);  // (slot >> 5) & 7 for slots 8l..8l+7
 #pragma unroll
         for (uint32_t k = 0; k < 8; k++)
-            if (k < kmax) sA[i0 + k] = make_uint2(re[k], first + sk[k] + span - 1);
+            if (k < kmax) {
+                sW[(i0 + k) ^ swz] = base[k] + jk[k];
+                sW[256 + ((i0 + k) ^ swz)] = sk[k];
+            }
+    }
+    __syncwarp();
+    {
+        uint32_t pi[8], sv[8];
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++) {
+            const uint32_t s = (uint32_t)lane + 32u * k;
+            if (s < count) {
+                pi[k] = sW[s ^ k];
+                sv[k] = sW[256 + (s ^ k)];
+            }
+        }
+        __syncwarp();  // every staging word is read before the slots are written
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++)
+            if ((uint32_t)lane + 32u * k < count) pi[k] = __ldcs(pos + pi[k]);
+#pragma unroll
+        for (uint32_t k = 0; k < 8; k++)
+            if ((uint32_t)lane + 32u * k < count) sA[lane + 32u * k] = make_uint2(pi[k], first + sv[k] + span - 1);
     }
     const uint32_t tlo = sa.tab_lo, thi = sa.tab_hi;
     const int X = sa.xdrop, T = sa.T;
