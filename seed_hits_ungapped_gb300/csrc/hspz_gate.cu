@@ -211,11 +211,19 @@ __device__ __forceinline__ void side_lead(WalkState &w, bool walk, uint32_t tlo,
     if (__all_sync(kFullMask, w.rem == 0u || w.rem > 8u * LEAD)) {
         // no walk of the round can reach its edge during the lead steps
         uint32_t keep = w.rem ? 0xFFFFFFFFu : 0u;
+        if constexpr (HAS_N) {
+            // the steps that test for N are longer: a partly rolled loop keeps
+            // the code within the instruction cache
+#pragma unroll 4
+            for (int i = 0; i < LEAD; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
+        } else {
 #pragma unroll
-        for (int i = 0; i < LEAD; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
+            for (int i = 0; i < LEAD; i++) walk_step_inner<HAS_N, BACK>(w, keep, tlo, thi, tab, X, need);
+        }
         w.rem = keep ? w.rem - 8u * LEAD : 0u;
     } else {
-#pragma unroll
+        // rounds near a sequence edge are rare: a rolled loop keeps the code small
+#pragma unroll 1
         for (int i = 0; i < LEAD; i++) walk_step_lead<HAS_N, BACK>(w, tlo, thi, tab, X, need);
     }
 }
