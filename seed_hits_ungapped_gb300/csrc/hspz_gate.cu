@@ -380,27 +380,41 @@ constexpr int kWUnit = 256;            // anchor slots per warp
 constexpr int kWTile = kWWarps * kWUnit;
 constexpr int kWSeeds = 1024;          // cached seed prefixes per CTA
 
-// The seeds of the first and last anchor slot of every tile (thread per tile).
+// The seeds of the first and last anchor slot of every tile, one thread per
+// tile boundary b (anchor a = min(n, 1024 b) of the chunk): the last seed of
+// tile b - 1 is the first seed whose prefix reaches hb + a, and the first seed
+// of tile b the first whose prefix passes it, which is the same seed unless a
+// seed ends exactly at the boundary.  So one binary search serves both.
 __global__ void k_tile_seeds(const uint32_t *__restrict__ P, uint32_t sb, uint32_t se, uint32_t hb, uint64_t n_hits,
                              uint64_t n_tiles, uint32_t *__restrict__ tiles) {
-    for (uint64_t t = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; t < n_tiles;
-         t += (uint64_t)gridDim.x * blockDim.x) {
-        const uint64_t s0 = t * kWTile, s1 = min(n_hits, s0 + kWTile) - 1;
-        const uint32_t a = upper_bound_g(P, sb, se, hb + (uint32_t)s0);
-        tiles[2 * t] = a;
-        tiles[2 * t + 1] = upper_bound_g(P, a, se, hb + (uint32_t)s1);
+    for (uint64_t b = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; b <= n_tiles;
+         b += (uint64_t)gridDim.x * blockDim.x) {
+        const uint32_t key = hb + (uint32_t)min(n_hits, b * (uint64_t)kWTile);
+        uint32_t first;
+        if (b == 0) {
+            first = upper_bound_g(P, sb, se, key);
+        } else {
+            const uint32_t last = upper_bound_g(P, sb, se, key - 1);
+            tiles[2 * b - 1] = last;
+            if (b == n_tiles) continue;
+            first = __ldg(P + last) > key ? last : upper_bound_g(P, last, se, key);
+        }
+        tiles[2 * b] = first;
     }
 }
 
 // Fused expansion + gate.  The CTA owns kWTile consecutive anchor slots and
-// caches the prefixes of the seeds they come from; after that one barrier
+// caches the prefixes of the seeds they come from (and their bucket starts,
+// when the tile spans at most kWSeeds / 2 seeds); after that one barrier
 // every warp works alone on its own 256 slots:
-//   1. lane l expands slots 8l..8l+7 of the warp's share into shared memory
-//      (search for the first slot's seed, then walk forward);
-//   2. the gate runs in 8 synchronous rounds of 32 anchors (one per lane,
-//      gate_round): all lanes walk their left sides together, first a fixed
-//      number of branch-free steps, then single steps under a warp vote
-//      while any lane still walks; then their right sides the same way;
+//   1. lane l finds the seed and occurrence of slots 8l..8l+7 of the warp's
+//      share (search for the first slot's seed, then walk forward), then the
+//      positions of slots l + 32k are loaded into shared memory;
+//   2. the gate runs in 8 synchronous rounds of 32 anchors (one per lane):
+//      all lanes walk their left sides together, first a fixed number of
+//      branch-free steps, then single steps under a warp vote while any lane
+//      still walks; then their right sides the same way (EXACT: a few lead
+//      steps, with the longer right walks deferred and finished 32 at a time);
 //   3. the warp stores its flags (per round) and anchors with coalesced,
 //      cache-streaming writes.
 template <bool HAS_N, bool EXACT>
@@ -418,8 +432,18 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     if (tid < 25) tab[tid] = sa.m[tid];
     const uint32_t first = __ldg(tiles + 2 * (uint64_t)blockIdx.x), ns = __ldg(tiles + 2 * (uint64_t)blockIdx.x + 1) - first + 1;
     const bool cached = ns <= (uint32_t)kWSeeds;
-    if (cached)
+    // a tile of at most kWSeeds / 2 seeds (the usual case) caches their bucket
+    // starts too, in the upper half, loaded together with the prefixes
+    const bool lo_cached = ns <= (uint32_t)kWSeeds / 2;
+    const uint32_t *sL = sP + kWSeeds / 2;
+    if (lo_cached) {
+        for (uint32_t i = tid; i < ns; i += kWWarps * 32) {
+            sP[i] = __ldg(P + first + i);
+            sP[kWSeeds / 2 + i] = __ldg(lo + first + i);
+        }
+    } else if (cached) {
         for (uint32_t i = tid; i < ns; i += kWWarps * 32) sP[i] = __ldg(P + first + i);
+    }
     __syncthreads();
     const uint32_t wbase = (uint32_t)warp * kWUnit;  // this warp's slots within the tile
     // with EXACT every warp reaches the barrier after the expansion, even one without slots
@@ -429,8 +453,9 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
     uint2 *sA = sA_all + wbase;
 
     // 1. expansion.  The lane first finds the seed and occurrence of each of
-    // its 8 consecutive slots (from the cached prefixes) and issues their 8
-    // bucket-start loads together; the position indices then pass through
+    // its 8 consecutive slots (from the cached prefixes) and takes their 8
+    // bucket starts from the cache, or issues their 8 loads together when the
+    // tile's bucket starts are not cached; the position indices then pass through
     // shared memory, so that lane l loads the positions of slots l + 32k:
     // each load instruction covers 32 consecutive anchors (a few buckets)
     // rather than 32 buckets.  The staging words sit in the warp's anchor
@@ -465,7 +490,15 @@ __global__ void __launch_bounds__(kWWarps * 32, HSPZ_GATE_MIN_BLOCKS)
         }
         uint32_t base[8];
 #pragma unroll
-        for (uint32_t k = 0; k < 8; k++) base[k] = __ldg(lo + first + sk[k]);
+        for (uint32_t k = 0; k < 8; k++) base[k] = sk[k];
+        if (lo_cached) {
+#pragma unroll
+            for (uint32_t k = 0; k < 8; k++) base[k] = sL[base[k]];
+        } else {
+#pragma unroll
+            for (uint32_t k = 0; k < 8; k++) base[k] = __ldg(lo + first + base[k]);
+        }
+
         const uint32_t swz = (uint32_t)(lane >> 2);  // (slot >> 5) & 7 for slots 8l..8l+7
 #pragma unroll
         for (uint32_t k = 0; k < 8; k++)
@@ -613,7 +646,7 @@ cudaError_t launch_expand_gate(const uint32_t *d_P, const uint32_t *d_lo, const 
         k_expand_gate<false><<<g, kFuseThreads, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), sa, out, d_flags); count_launch();
     } else if (sa.fast) {
         const uint64_t n_tiles = (n + kWTile - 1) / kWTile;
-        k_tile_seeds<<<(unsigned)((n_tiles + 255) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
+        k_tile_seeds<<<(unsigned)((n_tiles + 256) / 256), 256, 0, st>>>(d_P, sb, se, hb, n, n_tiles, d_tiles); count_launch();
         auto kern = sa.exact ? (ref.has_n || qry.has_n ? k_expand_gate_w<true, true> : k_expand_gate_w<false, true>)
                              : (ref.has_n || qry.has_n ? k_expand_gate_w<true, false> : k_expand_gate_w<false, false>);
         kern<<<(unsigned)n_tiles, kWWarps * 32, 0, st>>>(d_P, d_lo, d_pos, sb, se, hb, n, span, seqs(ref, qry), d_tiles, sa,

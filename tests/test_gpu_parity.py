@@ -348,6 +348,44 @@ def test_process_chunk_capacity_and_counts(torch_cuda):
     assert np.array_equal(big[3][:na].cpu().numpy().view(np.uint32), orc["accepted"])
 
 
+def test_process_chunk_ragged_unaligned_short(torch_cuda):
+    """hspz_process_chunk (C.5 through E.5 with the D.4 compactions) on chunks
+    of ragged sizes, with the flag buffer at an odd address (the byte-load
+    path of the compaction) and with a survivor buffer one slot short of the
+    count (capacity error with the needed count)."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    w = synth.make("tiny", scale=0.3)
+    max_hits = 1000
+    eng = _engine(torch, w.ref, w.matrix, w.xdrop, w.K)
+    plan = eng.plan(_dev(torch, w.query), max_hits)
+    orc = oracle.run_path(w.ref, w.query, w.matrix, w.xdrop, w.K, max_hits=max_hits)
+    assert np.array_equal(plan.chunks, orc["chunks"]) and len(orc["per_chunk"]) > 3
+    sizes = set()
+    for ci, pc in enumerate(orc["per_chunk"]):
+        n = pc["flags"].size
+        sizes.add(n % 256)
+        anchors = torch.empty((n, 2), dtype=torch.int32, device="cuda")
+        flags = torch.full((n + 1,), 7, dtype=torch.uint8, device="cuda")[1:]
+        m = pc["ids"].size
+        bufs = [torch.full((m + 1,), -3, dtype=torch.int32, device="cuda"),
+                torch.empty((m + 1, 4), dtype=torch.int32, device="cuda"),
+                torch.empty(m + 1, dtype=torch.uint8, device="cuda"),
+                torch.empty(m + 1, dtype=torch.int32, device="cuda")]
+        ns, na, _ = hspz.hspz_process_chunk(plan, ci, eng.params, anchors, flags, *bufs)
+        assert ns == m and na == pc["accepted"].size
+        assert np.array_equal(flags.cpu().numpy(), pc["flags"])
+        assert np.array_equal(bufs[0][:m].cpu().numpy().view(np.uint32), pc["ids"])
+        assert int(bufs[0][m]) == -3
+        assert np.array_equal(bufs[1][:m].cpu().numpy(), pc["rec"])
+        if m:
+            short = [b[:m - 1] for b in bufs]
+            with pytest.raises(hspz.HspzError) as e:
+                hspz.hspz_process_chunk(plan, ci, eng.params, anchors, flags, *short)
+            assert e.value.needed == m
+    assert len(sizes) > 1  # chunk ends fall at different places of a 256-anchor block
+
+
 def test_materialize_any_id_order(torch_cuda):
     """E.1-E.5 per survivor, whatever the id list: ascending survivors (long
     runs of neighbours on one diagonal), reversed, shuffled, with duplicates,
