@@ -79,16 +79,20 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms from before
+    the warm-up on; the summary keeps the samples whose timestamps fall in
+    the timed region (`window`, wall-clock seconds)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index: int, path: str | None = None):
         import tempfile
         self.gpu = gpu_index
         self.proc = None
+        self.window = None
         self.path = path or os.path.join(tempfile.gettempdir(), "hspz_bench_clocks_%d_gpu%d.csv"
                                          % (os.getpid(), gpu_index))
 
@@ -97,7 +101,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -115,19 +119,35 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) >= 9:
-                rows.append(parts)
+            if len(parts) < 10:
+                continue
+            try:  # nvidia-smi prints local time, e.g. 2026/12/02 19:59:03.123
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                continue
+            rows.append((ts, parts[1:]))
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        where = "all samples"
+        if self.window is not None:
+            slack = self.INTERVAL_MS / 1e3
+            inside = [r for r in rows if self.window[0] - slack <= r[0] <= self.window[1] + slack]
+            if inside:
+                rows, where = inside, "timed region"
+            else:  # a region shorter than the sampling interval: the nearest sample
+                mid = 0.5 * (self.window[0] + self.window[1])
+                rows, where = [min(rows, key=lambda r: abs(r[0] - mid))], "nearest to the timed region"
+        vals = [r[1] for r in rows]
+        sm = [float(v[1]) for v in vals if v[1].replace(".", "").isdigit()]
+        mx = [float(v[2]) for v in vals if v[2].replace(".", "").isdigit()]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        reasons = sorted({names[k] for v in vals for k in range(4) if v[5 + k].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(vals), "sampled": where}
 
 
 def host_info():
@@ -228,7 +248,7 @@ def reference_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--workload", default="workload_a")
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
@@ -308,17 +328,19 @@ def main():
             plan.close()
         return n_anchors, n_seeds
 
-    for _ in range(args.warmup):
-        step()
-    barrier()
-
-    # timed region: K steps, each bracketed by CUDA events on the launching
-    # stream, with an L2 flush between steps outside the events
-    step_ms = []
-    launches0 = lib.hspz_kernel_launches()
+    # clock samples run from before the warm-up on (nvidia-smi takes a while
+    # to start); the summary keeps those inside the timed region
     with ClockSampler(local, args.clocks_csv) as clocks:
+        for _ in range(args.warmup):
+            step()
         barrier()
-        t_wall0 = time.perf_counter()
+
+        # timed region: K steps, each bracketed by CUDA events on the launching
+        # stream, with an L2 flush between steps outside the events
+        step_ms = []
+        launches0 = lib.hspz_kernel_launches()
+        barrier()
+        t_wall0, t_epoch0 = time.perf_counter(), time.time()
         for _ in range(args.steps):
             flush.zero_()
             a = torch.cuda.Event(enable_timing=True)
@@ -330,6 +352,7 @@ def main():
             step_ms.append(a.elapsed_time(b))
         barrier()
         t_wall = time.perf_counter() - t_wall0
+        clocks.window = (t_epoch0, time.time())
     launches = lib.hspz_kernel_launches() - launches0
     total_ms = sum(step_ms)
     if world > 1:

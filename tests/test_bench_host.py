@@ -44,3 +44,30 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_only(src) == 'int a = 1; const char *s = "//x /*y*/"; int b = a + 1;'
     assert bench.code_only(src.replace("// walk", "// other words")) == bench.code_only(src)
     assert bench.code_only(src.replace("a + 1", "a + 2")) != bench.code_only(src)
+
+
+def test_clock_summary_keeps_samples_of_the_timed_region(tmp_path):
+    """The clock record keeps the nvidia-smi samples whose timestamps fall in
+    the timed region; a region shorter than the sampling interval takes the
+    nearest sample."""
+    import datetime
+    path = tmp_path / "clocks.csv"
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5, 0)
+    lines = []
+    for i, (mhz, cap) in enumerate([(1400, "Active"), (2070, "Not Active"), (2070, "Not Active"),
+                                    (1980, "Not Active"), (1200, "Active")]):
+        ts = (t0 + datetime.timedelta(milliseconds=500 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        lines.append("%s, 0, %d, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, %s" % (ts, mhz, cap))
+    path.write_text("\n".join(lines) + "\n")
+    c = bench.ClockSampler(0, str(path))
+    c.proc = object()  # as if nvidia-smi had run
+    base = t0.timestamp()
+    c.window = (base + 0.45, base + 1.55)  # samples 1, 2 and 3
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2070 and s["reasons"] == [] and s["sampled"] == "timed region"
+    c.window = (base + 2.2, base + 2.21)  # after the last sample (2.0 s): that one
+    s = c.summary()
+    assert s["samples"] == 1 and s["sm_mhz"] == 1200 and s["reasons"] == ["sw_power_cap"]
+    c.window = None
+    s = c.summary()
+    assert s["samples"] == 5 and s["reasons"] == ["sw_power_cap"] and s["sm_max_mhz"] == 2070
