@@ -438,7 +438,8 @@ def test_run_stream_batches_match_oracle(torch_cuda):
     """HspEngine.run_stream: uploads and result copies on a copy stream,
     overlapping the next batch.  Every batch, chunk by chunk, must hold the
     oracle's records, done flags and accepted ids; several chunks per batch
-    (MAX_HITS cuts) make the two result sets alternate within a batch."""
+    (MAX_HITS cuts) make the two result sets alternate within a batch.  A
+    consumer that stops early leaves the engine usable."""
     torch = torch_cuda
     w = synth.make("tiny")
     m = w.matrix
@@ -457,6 +458,13 @@ def test_run_stream_batches_match_oracle(torch_cuda):
                 assert np.array_equal(g.accepted, o["accepted"])
             got += 1
         assert got == len(qs)
+    gen = eng.run_stream(pinned, max_hits=0)
+    next(gen)
+    gen.close()  # the second batch's upload was already under way
+    res = next(eng.run_stream(pinned[1:2], max_hits=0))
+    orc = oracle.run_path(w.ref, qs[1], m, w.xdrop, w.K)
+    assert res.total_hits == orc["total"]
+    assert all(np.array_equal(g.records, o["rec"]) for g, o in zip(res.per_chunk, orc["per_chunk"]))
 
 
 def test_repetitive_chunks_group_by_diagonal(torch_cuda):
