@@ -200,6 +200,23 @@ def test_edges(torch_cuda):
     assert gpu.total_hits == 0 and orc["total"] == 0
 
 
+def test_xdrop_and_threshold_extremes(torch_cuda):
+    """Degenerate scoring parameters, everything equal to the oracle: X = 0
+    (a walk stops at its first fall below its maximum; the 8-base stop test
+    is not exact there), K = 1 (the keep threshold every anchor with a
+    positive side reaches, so nearly every flag is set and the compactions
+    see dense flags) and a threshold no anchor reaches (nothing survives)."""
+    w = synth.make("tiny", scale=0.2)
+    seen = {}
+    for xdrop, K in ((0, 3000), (910, 1), (0, 1), (910, 10 ** 7)):
+        gpu, orc = run_both(torch_cuda, w.ref, w.query, w.matrix, xdrop, K, max_hits=3000)
+        assert_same_as_oracle(gpu, orc)
+        flags = np.concatenate([pc["flags"] for pc in orc["per_chunk"]])
+        seen[(xdrop, K)] = flags.mean()
+    assert seen[(910, 1)] > 0.95 and seen[(910, 10 ** 7)] == 0.0
+    assert seen[(0, 1)] > 0.5
+
+
 def test_expansion_mappings_and_standalone_gate(torch_cuda):
     """C.4: sparse and dense mappings give the fused kernel's anchors; the
     standalone gate over those anchors gives the fused flags."""
