@@ -217,6 +217,22 @@ def test_xdrop_and_threshold_extremes(torch_cuda):
     assert seen[(0, 1)] > 0.5
 
 
+@pytest.mark.parametrize("pattern,scale,max_hits", [
+    ("11111111111", 0.2, 0),                                  # contiguous 11-mer
+    ("111010010100110111", 0.2, 0),                           # another spaced seed
+    ("1101011", 0.05, 100_000),                               # weight 5: ~50 hits per seed, chunked
+    ("11100000000000000000000000000111", 0.2, 400_000),       # the longest span (32), weight 6
+])
+def test_other_seed_patterns(torch_cuda, pattern, scale, max_hits):
+    """C.1-E.5 with seed patterns other than 12of19 (any weight up to 12 and
+    span up to 32 is accepted): index, counts, prefix, chunks, anchors,
+    flags, survivors and records all equal the oracle's."""
+    w = synth.make("tiny", scale=scale)
+    gpu, orc = run_both(torch_cuda, w.ref, w.query, w.matrix, w.xdrop, w.K, max_hits=max_hits, pattern=pattern)
+    assert orc["total"] > 0
+    assert_same_as_oracle(gpu, orc)
+
+
 def test_expansion_mappings_and_standalone_gate(torch_cuda):
     """C.4: sparse and dense mappings give the fused kernel's anchors; the
     standalone gate over those anchors gives the fused flags."""
