@@ -179,6 +179,27 @@ def test_fast_gate_both_step_tests(torch_cuda, name, scale, xdrop, K):
     plan.close()
 
 
+@pytest.mark.parametrize("xdrop", [889, 888, 2000])
+def test_fast_gate_int8_extreme_matrix(torch_cuda, xdrop):
+    """The table-scored path with pair scores at the ends of int8 (A/T match
+    +127, C/G match +120, transitions -60, transversions -128, N -100):
+    exact 8-base stop test from X = 7 * 127 = 889 up, base-by-base replay
+    below; every output equal to the oracle (mid scaled: N runs in both
+    sequences)."""
+    m = np.full((5, 5), -128, dtype=np.int32)
+    for r, q in ((0, 2), (2, 0), (1, 3), (3, 1)):
+        m[r, q] = -60
+    m[0, 0] = m[3, 3] = 127
+    m[1, 1] = m[2, 2] = 120
+    m[4, :] = m[:, 4] = -100
+    assert all(m[r, q] == m[r ^ 3, q ^ 3] for r in range(4) for q in range(4))  # complement symmetric
+    w = synth.make("mid", scale=0.1)
+    gpu, orc = run_both(torch_cuda, w.ref, w.query, m, xdrop, 3000, max_hits=20_000)
+    flags = np.concatenate([pc["flags"] for pc in orc["per_chunk"]])
+    assert 0 < flags.sum() < flags.size
+    assert_same_as_oracle(gpu, orc)
+
+
 def test_edges(torch_cuda):
     rng = np.random.default_rng(11)
     m = synth.hoxd70()
