@@ -90,3 +90,40 @@ def test_raw_gate_and_materialize_match_oracle(torch_cuda, which):
     assert np.array_equal(done.cpu().numpy(), done_o)
     assert np.array_equal(out.cpu().numpy(), rec_o)
     assert done_o.sum() == surv.size  # every survivor is accepted (done = score >= T)
+
+
+@pytest.mark.parametrize("X", [910, 600])
+def test_walks_past_2_pow_20_steps_match_oracle(torch_cuda, X):
+    """E.2/E.3 on sides longer than 2^20 steps of 8 bases, where the 32-bit
+    running sum of the 8-base walk hands the survivor over to the 64-bit
+    base-by-base walk: 17 Mbp sequences that agree everywhere but at a few
+    scattered bases, anchors in the middle (both sides ~8.5 Mbp), near the
+    start (right side ~17 Mbp) and on one diagonal a few bases apart (joined
+    walks), with the exact 8-base stop test (X = 910) and the replayed one
+    (X = 600).  Records and flags equal the oracle's."""
+    from seed_hits_ungapped_gb300 import hspz
+    torch = torch_cuda
+    rng = np.random.default_rng(77)
+    L = 17_000_000
+    ref = rng.integers(0, 4, L).astype(np.uint8)
+    qry = ref.copy()
+    mis = rng.choice(L, 40, replace=False)
+    qry[mis] = (qry[mis] + 1) % 4
+    m, K = synth.hoxd70(), 3000
+    T = oracle.keep_threshold(K)
+    a = np.array([[L // 2, L // 2], [L // 2 + 37, L // 2 + 37], [100, 100], [L - 50, L - 50]], np.uint32)
+    d_ref, d_qry = torch.from_numpy(ref).cuda(), torch.from_numpy(qry).cuda()
+    d_a = torch.from_numpy(a.view(np.int32)).cuda()
+    params = hspz.score_params(m, X, K)
+    flags = torch.full((a.shape[0],), 7, dtype=torch.uint8, device="cuda")
+    hspz.hspz_score_gate(d_a, a.shape[0], d_ref, d_qry, params, flags)
+    assert np.array_equal(flags.cpu().numpy(), oracle.gate(ref, qry, a, m, X, T))
+    ids = np.arange(a.shape[0], dtype=np.uint32)
+    rec_o, done_o = oracle.materialize(ref, qry, a, 0, ids, m, X, T)
+    assert rec_o[0, 2] > 8 * (1 << 21)  # both sides of the middle anchor pass 2^20 steps
+    out = torch.full((ids.size, 4), -3, dtype=torch.int32, device="cuda")
+    done = torch.full((ids.size,), 9, dtype=torch.uint8, device="cuda")
+    hspz.hspz_materialize(d_a, 0, torch.from_numpy(ids.view(np.int32)).cuda(), ids.size, d_ref, d_qry, params, out,
+                          done)
+    assert np.array_equal(done.cpu().numpy(), done_o)
+    assert np.array_equal(out.cpu().numpy(), rec_o)
