@@ -72,6 +72,45 @@ cudaError_t pool_alloc(void **p, size_t bytes, cudaStream_t st) {
 
 cudaError_t pool_free(void *p, cudaStream_t st) { return p ? cudaFreeAsync(p, st) : cudaSuccess; }
 
+namespace {
+// Small results (totals, counts) come back to the host through pinned,
+// device-mapped host memory that a one-thread kernel writes, not through a
+// device-to-host copy: on the copy engine such a copy waits behind the large
+// downloads queued before it on other streams (a streamed batch's results,
+// tens of GB on dense), which held the next batch's planning for ~0.3 s.
+__global__ void k_read_back(const uint64_t *__restrict__ src, volatile uint64_t *dst, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+    __threadfence_system();
+}
+
+// One staging area per host thread (a call launches and collects on the same
+// thread); kept for the thread's lifetime.
+thread_local uint64_t *tl_read_back = nullptr;
+}  // namespace
+
+cudaError_t read_back_launch(const uint64_t *d_src, int n, cudaStream_t st) {
+    if (n < 1 || n > 8) return cudaErrorInvalidValue;
+    if (!tl_read_back) {
+        uint64_t *h = nullptr;
+        cudaError_t e = cudaHostAlloc(reinterpret_cast<void **>(&h), 64, cudaHostAllocMapped | cudaHostAllocPortable);
+        if (e != cudaSuccess) return e;
+        tl_read_back = h;
+    }
+    uint64_t *d = nullptr;
+    cudaError_t e = cudaHostGetDevicePointer(reinterpret_cast<void **>(&d), tl_read_back, 0);
+    if (e != cudaSuccess) return e;
+    k_read_back<<<1, 32, 0, st>>>(d_src, d, n); count_launch();
+    return cudaGetLastError();
+}
+
+cudaError_t read_back_finish(uint64_t *host, int n, cudaStream_t st) {
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    const volatile uint64_t *h = tl_read_back;
+    for (int i = 0; i < n; i++) host[i] = h[i];
+    return cudaSuccess;
+}
+
 static std::atomic<uint64_t> g_launches{0};
 void count_launch(uint64_t k) { g_launches.fetch_add(k, std::memory_order_relaxed); }
 
@@ -349,8 +388,8 @@ int hspz_find_hits(const hspz_index *ix, const uint8_t *d_query, uint64_t query_
     if (e == cudaSuccess && S) e = launch_scan_u64(bsum, nb, bexcl, bincl, dtot, st);
     if (e == cudaSuccess && S) e = launch_prefix(p->d_cnt, S, bexcl, p->d_P, st);
     uint64_t tot_n[2] = {0, 0};
-    if (e == cudaSuccess) e = cudaMemcpyAsync(tot_n, dtot, 16, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = read_back_launch(dtot, 2, st);
+    if (e == cudaSuccess) e = read_back_finish(tot_n, 2, st);
     const uint64_t total = tot_n[0];
     p->has_n = tot_n[1] != 0;
     if (e != cudaSuccess) {
@@ -513,10 +552,10 @@ int hspz_process_chunk(const hspz_plan *p, uint32_t chunk, const hspz_score_para
     } else if (e == cudaSuccess) {
         e = cudaMemsetAsync(tot + 1, 0, 8, st);
     }
-    if (e == cudaSuccess) e = cudaMemcpyAsync(totals, tot, 16, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = read_back_launch(tot, 2, st);  // before the scratch holding them is freed
     cudaError_t ef = scratch ? pool_free(scratch, st) : cudaSuccess;
     if (e == cudaSuccess) e = ef;
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = read_back_finish(totals, 2, st);
     if (e == cudaSuccess && gate_ms) e = cudaEventElapsedTime(gate_ms, ev0, ev1);
     if (ev0) cudaEventDestroy(ev0);
     if (ev1) cudaEventDestroy(ev1);
@@ -624,10 +663,10 @@ int hspz_compact(const uint8_t *d_flags, uint64_t n, uint32_t id_base, uint32_t 
     uint64_t *d_total = reinterpret_cast<uint64_t *>(scratch + ((words - 2) & ~1ull));
     uint64_t total = 0;
     e = launch_compact(d_flags, n, id_base, d_ids, cap, scratch, d_total, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&total, d_total, 8, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = read_back_launch(d_total, 1, st);  // before the scratch holding it is freed
     cudaError_t ef = pool_free(scratch, st);
     if (e == cudaSuccess) e = ef;
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = read_back_finish(&total, 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_compact");
     *n_out = total;
     return total > cap ? HSPZ_E_CAPACITY : HSPZ_OK;
@@ -665,10 +704,10 @@ int hspz_dedup(const hspz_segment_pair *d_records, uint64_t n, uint32_t *d_keep_
     if (e == cudaSuccess)
         e = launch_dedup(d_records, n, d_tab, slots, d_keep, reinterpret_cast<unsigned long long *>(d_tail + 1), st);
     if (e == cudaSuccess) e = launch_compact(d_keep, n, 0, d_keep_ids, cap, d_cs, d_tail, st);
-    if (e == cudaSuccess) e = cudaMemcpyAsync(tail, d_tail, 16, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = read_back_launch(d_tail, 2, st);  // before the scratch holding them is freed
     cudaError_t ef = pool_free(scratch, st);
     if (e == cudaSuccess) e = ef;
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e == cudaSuccess) e = read_back_finish(tail, 2, st);
     if (e != cudaSuccess) return cuda_fail(e, "hspz_dedup");
     if (tail[1]) {
         set_error("hspz_dedup: hash probe sequence exhausted");

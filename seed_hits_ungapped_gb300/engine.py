@@ -289,10 +289,10 @@ class HspEngine:
         """Query batches from host memory through the whole path, pipelined.
 
         `host_queries` is an iterable of uint8 CPU tensors (pinned, for the
-        copies to overlap).  While the compute stream works on batch i, a
-        copy stream brings batch i+1 to the device and takes each finished
-        chunk's results (records, done flags, accepted ids) back to pinned
-        host buffers.  Yields one BatchResult per batch, in order, once its
+        copies to overlap).  While the compute stream works on batch i, an
+        upload stream brings batch i+1 to the device and a copy stream takes
+        each finished chunk's results (records, done flags, accepted ids)
+        back to pinned host buffers.  Yields one BatchResult per batch, in order, once its
         results are on the host; its arrays stay valid until the generator is
         resumed.  Device query and result buffers alternate between two sets,
         so a set is reused only after its copies have finished (events on the
@@ -302,6 +302,11 @@ class HspEngine:
         cs = getattr(self, "_copy_stream", None)
         if cs is None:
             cs = self._copy_stream = torch.cuda.Stream()
+        # uploads get a stream of their own: behind a batch's downloads (43 GB
+        # on dense) the next batch's upload, and so its plan, would wait
+        us = getattr(self, "_upload_stream", None)
+        if us is None:
+            us = self._upload_stream = torch.cuda.Stream()
         dq = [None, None]
         ev_in = [None, None]
 
@@ -310,10 +315,10 @@ class HspEngine:
             have = dq[p]
             if have is None or have.numel() < n:
                 dq[p] = torch.empty(max(n, 1), dtype=torch.uint8, device="cuda")
-            with torch.cuda.stream(cs):
+            with torch.cuda.stream(us):
                 dq[p][:n].copy_(q, non_blocking=True)
                 ev_in[p] = torch.cuda.Event()
-                ev_in[p].record(cs)
+                ev_in[p].record(us)
             return n
 
         it = iter(host_queries)
