@@ -111,7 +111,12 @@ uint64_t hspz_kernel_launches(void);
  * the library; memory freed back to it stays cached for the next call instead
  * of being returned to the driver.  This returns every pool's cached memory
  * that no allocation holds (cudaMemPoolTrimTo).  Memory still held by live
- * plans or by frees not yet reached on their streams stays in the pools. */
+ * plans or by frees not yet reached on their streams stays in the pools.
+ * Calls that hand a count back to the host (hspz_find_hits,
+ * hspz_process_chunk, hspz_compact, hspz_dedup) read it through 64 bytes of
+ * pinned, device-mapped host memory that each calling thread allocates on
+ * its first such call and keeps for its lifetime (a one-thread kernel writes
+ * it, so the read does not queue behind large copies on the copy engine). */
 int hspz_release_cached_memory(void);
 
 /* ------------------------------------------------------------------------ *
