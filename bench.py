@@ -430,10 +430,16 @@ def main():
     # end to end through the public API with host buffers: HspEngine.run_stream
     # takes the pinned host batches and hands back each batch's results (records,
     # done flags, accepted ids of every chunk) in host memory; the next batch's
-    # upload and the finished chunks' downloads run on a copy stream while the
-    # compute stream works, so the copies of one batch overlap the next batch
+    # upload and the finished chunks' downloads run on their own streams while
+    # the compute stream works, so the copies of one batch overlap the next batch
     e2e = None
     if not args.no_e2e:
+        # the dedup leg's buffers (on dense, 33 GB of collected records) are not
+        # part of this path: hand their memory back before it runs
+        eng.release_buffers("batch_records", "final_ids")
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        hspz.hspz_release_cached_memory()
         pinned = [torch.from_numpy(q).pin_memory() for q in w.queries]
         h2d = sum(q.numel() for q in pinned)
         n_e2e = max(3, args.steps)

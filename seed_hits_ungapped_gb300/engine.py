@@ -162,6 +162,12 @@ class HspEngine:
             self._bufs[name] = new
         return self._bufs[name]
 
+    def release_buffers(self, *names):
+        """Drops the engine's named device buffers (every one when no name is
+        given); their memory goes back to PyTorch's caching allocator."""
+        for k in (names or tuple(self._bufs)):
+            self._bufs.pop(k, None)
+
     def dedup(self, d_records, n: int):
         """hspz_dedup into the engine's id buffer: (kept ids tensor, count)."""
         torch = self.torch
